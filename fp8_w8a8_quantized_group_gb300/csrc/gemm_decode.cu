@@ -1,0 +1,281 @@
+// Weight-streaming FP8 GEMM for decode-shaped problems (M <= 16 tokens).
+//
+// Decode reads every weight once per step and does little arithmetic per
+// byte, so it is bound by memory bandwidth ("FP8 serving slower than BF16",
+// section "Arithmetic Intensity: decode가 FP8을 살리지 못하는 이유"; "서빙을
+// 위한 양자화 가이드", item ② on decode being memory-bound). The design here:
+//
+//  - the weight matrix is the MMA's M side (128 weight rows per CTA) and the
+//    tokens are its N side (N = 16), so no tensor-core rows are spent on
+//    padding tokens to 128 and nothing padded is read from memory (the TMA
+//    fills token rows >= M with zeros on chip);
+//  - weights stream through a ring of TMA stages (16 KB of weights + 2 KB
+//    of activation codes per 128-wide K block), one lane issuing, so many
+//    bytes are in flight per SM with no register staging;
+//  - K is split across the CTAs of a thread-block cluster (up to 8) to put
+//    enough CTAs on the GPU; each CTA promotes its K blocks with the scales
+//    in FP32 registers, and the partial sums are reduced through distributed
+//    shared memory, each CTA of the cluster summing and storing a slice of
+//    the 128 rows. No global scratch memory is used.
+//
+// Block mode applies Sw[n/128][kb] * Sa[kb][m] per K block; per-tensor mode
+// accumulates all of the CTA's K range in TMEM and applies sa * sw once.
+#include <mutex>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace fp8k {
+namespace {
+
+constexpr int kRows = 128;      // weight rows per CTA (MMA M)
+constexpr int kTok = 16;        // token slots (MMA N)
+constexpr int BK = 128;
+constexpr int kStages = 6;
+constexpr int kWBytes = kRows * BK;
+constexpr int kXBytes = kTok * BK;
+constexpr int kThreads = 256;
+constexpr int kTmemCols = 32;   // two 16-column partial buffers
+constexpr int kRedStride = kTok + 1;
+constexpr int kSmemBytes = 1024 + kStages * (kWBytes + kXBytes) + 8 * (2 * kStages + 4) + 16;
+
+enum : unsigned { kSiteProdEmpty = 201, kSiteMmaTmem = 202, kSiteMmaFull = 203, kSiteEpiFull = 204,
+                  kSiteDrain = 205 };
+
+template <bool PER_TENSOR>
+__global__ void __launch_bounds__(kThreads, 2)
+    gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                       const float *__restrict__ sa, const float *__restrict__ sw,
+                       __nv_bfloat16 *__restrict__ y, int M, int N, int K, int splits, unsigned *err) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sW = smem;
+    uint8_t *sX = smem + kStages * kWBytes;
+    uint64_t *full = reinterpret_cast<uint64_t *>(sX + kStages * kXBytes);
+    uint64_t *empty = full + kStages;
+    uint64_t *tfull = empty + kStages;
+    uint64_t *tempty = tfull + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    float *red = reinterpret_cast<float *>(sW);  // reused after the main loop
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nb = blockIdx.x / splits;
+    const int split = blockIdx.x - nb * splits;
+    const int n0 = nb * kRows;
+    const int Kg = (K + BK - 1) / BK;
+    const int kb0 = static_cast<int>((static_cast<int64_t>(split) * Kg) / splits);
+    const int kb1 = static_cast<int>((static_cast<int64_t>(split + 1) * Kg) / splits);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+        for (int b = 0; b < 2; ++b) { mbar_init(&tfull[b], 1); mbar_init(&tempty[b], 128); }
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) { tma_prefetch_desc(&tmW); tma_prefetch_desc(&tmX); }
+    if (warp == 2) { tmem_alloc(tmem_slot, kTmemCols); tmem_relinquish(); }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    float acc[kTok];
+#pragma unroll
+    for (int j = 0; j < kTok; ++j) acc[j] = 0.0f;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // -------------------------------------------------- producer --
+            const uint64_t stream_once = policy_evict_first();
+            uint32_t stage = 0, phase = 0;
+            int issued = 0;
+            for (int kb = kb0; kb < kb1; ++kb) {
+                if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err, kSiteProdEmpty)) break;
+                mbar_arrive_expect_tx(&full[stage], kWBytes + kXBytes);
+                tma_load_2d_hint(sW + stage * kWBytes, &tmW, &full[stage], kb * BK, n0, stream_once);
+                tma_load_2d(sX + stage * kXBytes, &tmX, &full[stage], kb * BK, 0);
+                ++issued;
+                if (++stage == kStages) { stage = 0; phase ^= 1u; }
+            }
+            for (int i = 0; i < kStages && i < issued; ++i) {
+                if (stage == 0) { stage = kStages; phase ^= 1u; }
+                --stage;
+                const uint64_t t0 = global_ns();
+                while (!mbar_try_wait(&full[stage], phase)) {
+                    if (global_ns() - t0 > kWaitLimitNs) { record_error(err, kErrTimeout, kSiteDrain); break; }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------------- MMA --
+            constexpr uint32_t idesc = idesc_e4m3_f32(kRows, kTok);
+            uint32_t stage = 0, phase = 0, buf = 0, bphase = 0, last_stage = 0, last_phase = 0;
+            bool any = false;
+            for (int kb = kb0; kb < kb1; ++kb) {
+                const bool first = kb == kb0, last = kb == kb1 - 1;
+                if (!PER_TENSOR || first) {
+                    if (!mbar_wait(&tempty[buf], bphase ^ 1u, abort_flag, err, kSiteMmaTmem)) break;
+                    tc_fence_after();
+                }
+                if (!mbar_wait(&full[stage], phase, abort_flag, err, kSiteMmaFull)) break;
+                tc_fence_after();
+                const uint32_t w0 = smem_u32(sW + stage * kWBytes);
+                const uint32_t x0 = smem_u32(sX + stage * kXBytes);
+                const uint32_t d = tmem_base + buf * kTok;
+#pragma unroll
+                for (int k = 0; k < BK / 32; ++k) {
+                    const uint32_t accum = (k > 0 || (PER_TENSOR && !first)) ? 1u : 0u;
+                    umma_e4m3(d, sdesc_k_sw128(w0 + k * 32), sdesc_k_sw128(x0 + k * 32), idesc, accum);
+                }
+                umma_commit(&empty[stage]);
+                any = true;
+                last_stage = stage;
+                last_phase = phase;
+                if (!PER_TENSOR || last) {
+                    umma_commit(&tfull[buf]);
+                    if (++buf == 2) { buf = 0; bphase ^= 1u; }
+                }
+                if (++stage == kStages) { stage = 0; phase ^= 1u; }
+            }
+            if (any) {
+                const uint64_t t0 = global_ns();
+                while (!mbar_try_wait(&empty[last_stage], last_phase)) {
+                    if (global_ns() - t0 > kWaitLimitNs) { record_error(err, kErrTimeout, kSiteDrain); break; }
+                }
+            }
+        }
+    } else if (warp >= 4) {
+        // ---------------------------------------------------------- epilogue --
+        const int ep = warp - 4;
+        const int r = ep * 32 + lane;  // weight row within the CTA's 128
+        const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(ep * 32) << 16);
+        uint32_t buf = 0, bphase = 0;
+        if (!PER_TENSOR) {
+            const float *swrow = sw + static_cast<int64_t>(nb) * Kg;
+            for (int kb = kb0; kb < kb1; ++kb) {
+                const float wscale = __ldg(swrow + kb);
+                float sav[kTok];
+#pragma unroll
+                for (int j = 0; j < kTok; ++j) sav[j] = j < M ? __ldg(sa + static_cast<int64_t>(kb) * M + j) : 0.0f;
+                if (!__all_sync(0xffffffffu, mbar_wait(&tfull[buf], bphase, abort_flag, err, kSiteEpiFull))) break;
+                tc_fence_after();
+                float p[kTok];
+                tmem_ld16(lane_addr + buf * kTok, p);
+                tc_fence_before();
+                mbar_arrive(&tempty[buf]);
+                if (++buf == 2) { buf = 0; bphase ^= 1u; }
+#pragma unroll
+                for (int j = 0; j < kTok; ++j) acc[j] = fmaf(p[j], wscale * sav[j], acc[j]);
+            }
+        } else {
+            if (__all_sync(0xffffffffu, mbar_wait(&tfull[0], 0, abort_flag, err, kSiteEpiFull))) {
+                tc_fence_after();
+                float p[kTok];
+                tmem_ld16(lane_addr, p);
+                tc_fence_before();
+                const float sc = sa[0] * sw[0];
+#pragma unroll
+                for (int j = 0; j < kTok; ++j) acc[j] = p[j] * sc;
+            }
+        }
+        if (splits == 1) {
+            const int n = n0 + r;
+            if (n < N) {
+#pragma unroll
+                for (int j = 0; j < kTok; ++j)
+                    if (j < M) y[static_cast<int64_t>(j) * N + n] = __float2bfloat16_rn(acc[j]);
+            }
+        }
+    }
+
+    __syncwarp();  // lanes 1..31 of the producer and MMA warps wait for lane 0
+
+    if (splits > 1) {
+        // ------------------------------------- cluster split-K reduction --
+        // Every MMA has completed (the epilogue consumed the last partial, or
+        // the MMA lane drained), so the stage memory can hold the partials.
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncthreads();
+        if (warp >= 4) {
+            const int r = (warp - 4) * 32 + lane;
+#pragma unroll
+            for (int j = 0; j < kTok; ++j) red[r * kRedStride + j] = acc[j];
+        }
+        cluster_sync_all();
+        const uint32_t rank = cluster_ctarank();
+        const int rows_per = kRows / splits;
+        const int row0 = static_cast<int>(rank) * rows_per;
+        const uint32_t red_addr = smem_u32(red);
+        for (int idx = threadIdx.x; idx < rows_per * M; idx += kThreads) {
+            const int j = idx / rows_per;
+            const int row = row0 + (idx - j * rows_per);
+            const uint32_t off = static_cast<uint32_t>((row * kRedStride + j) * 4);
+            float sum = 0.0f;
+            for (int q = 0; q < splits; ++q) sum += ld_shared_cluster_f32(map_shared_rank(red_addr + off, q));
+            const int n = n0 + row;
+            if (n < N) y[static_cast<int64_t>(j) * N + n] = __float2bfloat16_rn(sum);
+        }
+        cluster_sync_all();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+template <bool PER_TENSOR>
+cudaError_t launch_variant(const void *qa, const float *sa, const void *qw, const float *sw, void *y, int64_t M,
+                           int64_t N, int64_t K, const DeviceInfo &dev, cudaStream_t stream) {
+    static std::once_flag attr_once[64];
+    static cudaError_t attr_err[64];
+    int device = 0;
+    cudaGetDevice(&device);
+    std::call_once(attr_once[device & 63], [&] {
+        cudaError_t e = cudaFuncSetAttribute(gemm_decode_kernel<PER_TENSOR>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        attr_err[device & 63] = e;
+    });
+    if (attr_err[device & 63] != cudaSuccess) return attr_err[device & 63];
+
+    CUtensorMap tmW, tmX;
+    if (encode_tma_2d_u8(&tmW, qw, K, N, K, BK, kRows) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    if (encode_tma_2d_u8(&tmX, qa, K, M, K, BK, kTok) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+
+    const int64_t nblocks = (N + kRows - 1) / kRows;
+    const int64_t Kg = (K + BK - 1) / BK;
+    // Split K over a cluster until about two CTAs per SM are in flight.
+    int splits = 1;
+    while (splits < 8 && nblocks * splits < 2 * dev.sm_count && splits * 2 <= Kg) splits *= 2;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(nblocks * splits));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(splits);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemm_decode_kernel<PER_TENSOR>, tmW, tmX, sa, sw,
+                              static_cast<__nv_bfloat16 *>(y), static_cast<int>(M), static_cast<int>(N),
+                              static_cast<int>(K), splits, dev.err);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_decode(const void *qa, const float *sa, const void *qw, const float *sw, void *y,
+                               int64_t M, int64_t N, int64_t K, bool per_tensor, const DeviceInfo &dev,
+                               cudaStream_t stream) {
+    if (per_tensor) return launch_variant<true>(qa, sa, qw, sw, y, M, N, K, dev, stream);
+    return launch_variant<false>(qa, sa, qw, sw, y, M, N, K, dev, stream);
+}
+
+}  // namespace fp8k

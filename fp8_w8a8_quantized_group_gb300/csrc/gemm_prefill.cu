@@ -1,0 +1,355 @@
+// Tile-persistent block-scaled FP8 GEMM for prefill-shaped (M > 16) and
+// grouped (mixture-of-experts) problems, sm_103a.
+//
+//   Y[m,n] = bf16( sum_g Sa[g][m] Sw[n/128][g] sum_{k in g} dec(Qa[m,k]) dec(Qw[n,k]) )
+//
+// The pages only fix what is computed: FP8 operands into the tensor cores
+// with high-precision accumulation ("FP8 and FP4: Throughput Needs Scaling",
+// section "Kernel caveat가 마지막 관문이다") and 128x128 weight blocks with
+// dynamic 128-groups for activations ("[vLLM] FP8", section "블록 양자화").
+// The kernel below is this library's own design for GB300:
+//
+//  - one CTA per SM, persistent over output tiles of 128 x BN;
+//  - warp 0 (one lane): TMA producer, fills a ring of shared-memory stages;
+//    one stage = one 128-wide K block of A (128 x 128 B) and B (BN x 128 B),
+//    both K-major with 128-byte swizzle;
+//  - warp 1 (one lane): issues 4 tcgen05.mma (K = 32 each) per stage into a
+//    fresh TMEM accumulator, so TMEM holds the FP32 partial of ONE K block;
+//    two TMEM buffers alternate so the MMA of block k+1 runs while block k
+//    is being promoted;
+//  - warps 4..7: epilogue, one thread per output row; per K block it loads
+//    the partial from TMEM and adds partial * (Sa * Sw) into FP32 registers
+//    (the per-block scale promotion), then writes BF16 at the end of the
+//    tile;
+//  - per-tensor mode: the MMAs accumulate all of K in TMEM and the single
+//    scale product is applied once per tile.
+//
+// Every wait is bounded (common.cuh); on expiry the CTA records an error,
+// stops issuing, lets the copies it issued land and frees its TMEM.
+#include <mutex>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace fp8k {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 128;  // one K block: one stage, 4 MMAs of K = 32
+constexpr int kThreads = 256;
+constexpr int kMaxGroups = 256;
+
+// Bounded-wait sites reported through the error word.
+enum : unsigned { kSiteProdEmpty = 101, kSiteMmaTmem = 102, kSiteMmaFull = 103, kSiteEpiFull = 104,
+                  kSiteDrain = 105 };
+
+template <int BN>
+struct Cfg {
+    static constexpr int kStages = 6;
+    static constexpr int kABytes = BM * BK;
+    static constexpr int kBBytes = BN * BK;
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kTmemCols = 2 * BN;
+    static constexpr int kBarrierBytes = 8 * (2 * kStages + 4) + 16;
+    static constexpr int kTableBytes = 4 * (3 * kMaxGroups + 2);
+    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarrierBytes + kTableBytes;
+};
+
+// Output tile of a linear tile index: rows [m0, m0+128) of which those below
+// row_end are written, columns [n0, n0+BN), B rows from b_row, expert group.
+struct Tile {
+    int m0, row_end, n0, b_row, group;
+};
+
+template <int BN>
+struct Sched {
+    int M, N, num_n, num_m, raster, groups;
+    const int *lo, *hi, *start;  // shared-memory tables (grouped only)
+
+    __device__ __forceinline__ Tile get(int t) const {
+        Tile r;
+        int mt, nt;
+        if (groups == 0) {
+            if (raster == 0) { mt = t / num_n; nt = t - mt * num_n; }
+            else             { nt = t / num_m; mt = t - nt * num_m; }
+            r.m0 = mt * BM;
+            r.row_end = M;
+            r.group = 0;
+        } else {
+            int e = 0;
+            while (e + 1 < groups && start[e + 1] <= t) ++e;
+            const int local = t - start[e];
+            mt = local / num_n;
+            nt = local - mt * num_n;
+            r.m0 = lo[e] + mt * BM;
+            r.row_end = hi[e];
+            r.group = e;
+        }
+        r.n0 = nt * BN;
+        r.b_row = r.group * N + r.n0;
+        return r;
+    }
+};
+
+template <int BN, bool PER_TENSOR>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const float *__restrict__ sa, const float *__restrict__ sw,
+                        __nv_bfloat16 *__restrict__ y, int M, int N, int K, int groups,
+                        const int32_t *__restrict__ offsets, int raster, unsigned *err) {
+    using C = Cfg<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + C::kStages * C::kABytes;
+    uint64_t *full = reinterpret_cast<uint64_t *>(sB + C::kStages * C::kBBytes);
+    uint64_t *empty = full + C::kStages;
+    uint64_t *tfull = empty + C::kStages;
+    uint64_t *tempty = tfull + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    int *t_lo = reinterpret_cast<int *>(tmem_slot + 4);
+    int *t_hi = t_lo + kMaxGroups;
+    int *t_start = t_hi + kMaxGroups;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int Kg = (K + BK - 1) / BK;
+    const int num_n = (N + BN - 1) / BN;
+    const int Nb = (N + 127) / 128;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+        for (int b = 0; b < 2; ++b) { mbar_init(&tfull[b], 1); mbar_init(&tempty[b], 128); }
+        *abort_flag = 0;
+        fence_barrier_init();
+        if (offsets != nullptr) {
+            // Expert e owns rows [lo, hi) clamped into [0, M]; its tiles follow
+            // those of experts < e (expert-major, n fastest within an expert).
+            int acc = 0;
+            for (int e = 0; e < groups; ++e) {
+                int lo = offsets[e], hi = offsets[e + 1];
+                lo = lo < 0 ? 0 : (lo > M ? M : lo);
+                hi = hi < lo ? lo : (hi > M ? M : hi);
+                t_lo[e] = lo;
+                t_hi[e] = hi;
+                t_start[e] = acc;
+                acc += ((hi - lo + BM - 1) / BM) * num_n;
+            }
+            t_start[groups] = acc;
+        }
+    }
+    if (warp == 0 && lane == 0) { tma_prefetch_desc(&tmA); tma_prefetch_desc(&tmB); }
+    if (warp == 2) { tmem_alloc(tmem_slot, C::kTmemCols); tmem_relinquish(); }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    Sched<BN> sched;
+    sched.M = M; sched.N = N; sched.num_n = num_n; sched.num_m = (M + BM - 1) / BM; sched.raster = raster;
+    sched.groups = offsets != nullptr ? groups : 0;
+    sched.lo = t_lo; sched.hi = t_hi; sched.start = t_start;
+    const int total = offsets != nullptr ? t_start[groups] : sched.num_m * num_n;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer --
+            uint32_t stage = 0, phase = 0;
+            int issued = 0;
+            for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
+                const Tile tl = sched.get(t);
+                for (int kb = 0; kb < Kg; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err, kSiteProdEmpty)) break;
+                    mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
+                    tma_load_2d(sA + stage * C::kABytes, &tmA, &full[stage], kb * BK, tl.m0);
+                    tma_load_2d(sB + stage * C::kBBytes, &tmB, &full[stage], kb * BK, tl.b_row);
+                    ++issued;
+                    if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+                }
+            }
+            // Let the last fill of every stage land before the CTA can exit
+            // (on the normal path these have all completed already).
+            for (int i = 0; i < C::kStages && i < issued; ++i) {
+                if (stage == 0) { stage = C::kStages; phase ^= 1u; }
+                --stage;
+                const uint64_t t0 = global_ns();
+                while (!mbar_try_wait(&full[stage], phase)) {
+                    if (global_ns() - t0 > kWaitLimitNs) { record_error(err, kErrTimeout, kSiteDrain); break; }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------- MMA issuer --
+            constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
+            uint32_t stage = 0, phase = 0, buf = 0, bphase = 0;
+            uint32_t last_stage = 0, last_phase = 0;
+            bool ok = true, any = false;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                for (int kb = 0; kb < Kg && ok; ++kb) {
+                    if (!PER_TENSOR || kb == 0) {
+                        ok = mbar_wait(&tempty[buf], bphase ^ 1u, abort_flag, err, kSiteMmaTmem);
+                        if (!ok) break;
+                        tc_fence_after();
+                    }
+                    ok = mbar_wait(&full[stage], phase, abort_flag, err, kSiteMmaFull);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(sA + stage * C::kABytes);
+                    const uint32_t b0 = smem_u32(sB + stage * C::kBBytes);
+                    const uint32_t d = tmem_base + buf * BN;
+#pragma unroll
+                    for (int k = 0; k < BK / 32; ++k) {
+                        const uint32_t acc = (k > 0 || (PER_TENSOR && kb > 0)) ? 1u : 0u;
+                        umma_e4m3(d, sdesc_k_sw128(a0 + k * 32), sdesc_k_sw128(b0 + k * 32), idesc, acc);
+                    }
+                    umma_commit(&empty[stage]);
+                    any = true;
+                    last_stage = stage;
+                    last_phase = phase;
+                    if (!PER_TENSOR || kb == Kg - 1) {
+                        umma_commit(&tfull[buf]);
+                        if (++buf == 2) { buf = 0; bphase ^= 1u; }
+                    }
+                    if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+                }
+            }
+            // The last commit arrives once every MMA issued here has finished
+            // reading shared memory and writing TMEM; wait for it before the
+            // CTA frees TMEM (already complete on the normal path).
+            if (any) {
+                const uint64_t t0 = global_ns();
+                while (!mbar_try_wait(&empty[last_stage], last_phase)) {
+                    if (global_ns() - t0 > kWaitLimitNs) { record_error(err, kErrTimeout, kSiteDrain); break; }
+                }
+            }
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------ epilogue --
+        const int ep = warp - 4;
+        const int r = ep * 32 + lane;
+        const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(ep * 32) << 16);
+        uint32_t buf = 0, bphase = 0;
+        float tensor_scale = 0.0f;
+        if (PER_TENSOR) tensor_scale = sa[0] * sw[0];
+        bool ok = true;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            const Tile tl = sched.get(t);
+            const int m = tl.m0 + r;
+            const bool row_in = m < M;
+            float acc[BN];
+#pragma unroll
+            for (int j = 0; j < BN; ++j) acc[j] = 0.0f;
+            if (!PER_TENSOR) {
+                const float *swg = sw + static_cast<int64_t>(tl.group) * Nb * Kg;
+                const int nb0 = tl.n0 / 128;
+                for (int kb = 0; kb < Kg; ++kb) {
+                    // scales for this K block (loads issued before the wait)
+                    const float sa_v = row_in ? __ldg(sa + static_cast<int64_t>(kb) * M + m) : 0.0f;
+                    float sw_v[(BN + 127) / 128];
+#pragma unroll
+                    for (int j = 0; j < (BN + 127) / 128; ++j)
+                        sw_v[j] = (nb0 + j < Nb) ? __ldg(swg + static_cast<int64_t>(nb0 + j) * Kg + kb) : 0.0f;
+                    ok = __all_sync(0xffffffffu, mbar_wait(&tfull[buf], bphase, abort_flag, err, kSiteEpiFull));
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int c = 0; c < BN / 32; ++c) {
+                        float p[32];
+                        tmem_ld32(lane_addr + buf * BN + c * 32, p);
+                        const float sc = sa_v * sw_v[(c * 32) / 128];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) acc[c * 32 + j] = fmaf(p[j], sc, acc[c * 32 + j]);
+                    }
+                    tc_fence_before();
+                    mbar_arrive(&tempty[buf]);
+                    if (++buf == 2) { buf = 0; bphase ^= 1u; }
+                }
+            } else {
+                ok = __all_sync(0xffffffffu, mbar_wait(&tfull[buf], bphase, abort_flag, err, kSiteEpiFull));
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c) {
+                    float p[32];
+                    tmem_ld32(lane_addr + buf * BN + c * 32, p);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) acc[c * 32 + j] = p[j] * tensor_scale;
+                }
+                tc_fence_before();
+                mbar_arrive(&tempty[buf]);
+                if (++buf == 2) { buf = 0; bphase ^= 1u; }
+            }
+            if (!ok) break;
+            if (m < tl.row_end && row_in) {
+                __nv_bfloat16 *yrow = y + static_cast<int64_t>(m) * N + tl.n0;
+#pragma unroll
+                for (int c = 0; c < BN / 8; ++c) {
+                    if (tl.n0 + c * 8 < N) {
+                        uint4 v;
+                        v.x = pack_bf16x2(acc[c * 8 + 0], acc[c * 8 + 1]);
+                        v.y = pack_bf16x2(acc[c * 8 + 2], acc[c * 8 + 3]);
+                        v.z = pack_bf16x2(acc[c * 8 + 4], acc[c * 8 + 5]);
+                        v.w = pack_bf16x2(acc[c * 8 + 6], acc[c * 8 + 7]);
+                        *reinterpret_cast<uint4 *>(yrow + c * 8) = v;
+                    }
+                }
+            }
+        }
+    }
+
+    __syncwarp();  // lanes 1..31 of the producer and MMA warps wait for lane 0
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::kTmemCols);
+    }
+}
+
+template <int BN, bool PER_TENSOR>
+cudaError_t launch_variant(const void *qa, const float *sa, const void *qw, const float *sw, void *y, int64_t M,
+                           int64_t N, int64_t K, int num_groups, const int32_t *offsets, const DeviceInfo &dev,
+                           cudaStream_t stream) {
+    using C = Cfg<BN>;
+    static std::once_flag attr_once[64];
+    static cudaError_t attr_err[64];
+    int device = 0;
+    cudaGetDevice(&device);
+    std::call_once(attr_once[device & 63], [&] {
+        attr_err[device & 63] = cudaFuncSetAttribute(gemm_prefill_kernel<BN, PER_TENSOR>,
+                                                     cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    });
+    if (attr_err[device & 63] != cudaSuccess) return attr_err[device & 63];
+
+    CUtensorMap tmA, tmB;
+    if (encode_tma_2d_u8(&tmA, qa, K, M, K, BK, BM) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    const int64_t b_rows = N * (offsets != nullptr ? num_groups : 1);
+    if (encode_tma_2d_u8(&tmB, qw, K, b_rows, K, BK, BN) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+
+    int64_t tiles;
+    const int64_t num_n = (N + BN - 1) / BN;
+    if (offsets == nullptr) tiles = ((M + BM - 1) / BM) * num_n;
+    else tiles = ((M + BM - 1) / BM + num_groups) * num_n;  // upper bound
+    const int64_t grid = tiles < dev.sm_count ? tiles : dev.sm_count;
+    if (grid <= 0) return cudaSuccess;
+    // Tiles sharing a row panel run together when the weight operand is the
+    // smaller one (it stays in L2 while activations stream), else the reverse.
+    const int raster = (N <= M) ? 0 : 1;
+    gemm_prefill_kernel<BN, PER_TENSOR><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(
+        tmA, tmB, sa, sw, static_cast<__nv_bfloat16 *>(y), static_cast<int>(M), static_cast<int>(N),
+        static_cast<int>(K), num_groups, offsets, raster, dev.err);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_prefill(const void *qa, const float *sa, const void *qw, const float *sw, void *y,
+                                int64_t M, int64_t N, int64_t K, int num_groups, const int32_t *offsets,
+                                bool per_tensor, const DeviceInfo &dev, cudaStream_t stream) {
+    if (per_tensor)
+        return launch_variant<128, true>(qa, sa, qw, sw, y, M, N, K, num_groups, offsets, dev, stream);
+    return launch_variant<128, false>(qa, sa, qw, sw, y, M, N, K, num_groups, offsets, dev, stream);
+}
+
+}  // namespace fp8k

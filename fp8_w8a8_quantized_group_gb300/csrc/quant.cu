@@ -1,0 +1,248 @@
+// Quantizer kernels: BF16 -> E4M3 codes + FP32 scales.
+//
+//  - 1 x 128 activation groups (dynamic, per token): one half-warp per group,
+//    16-byte loads of 8 BF16 per lane, shuffle amax over the half-warp,
+//    8-byte stores of 8 packed codes per lane.
+//  - 128 x 128 weight blocks: one CTA per block, the block held in registers
+//    between the amax pass and the quantize pass (read once).
+//  - Per tensor: grid-wide amax (atomicMax on the bit pattern of the
+//    non-negative amax, kept in the output scale slot), then quantize; a
+//    single-CTA kernel does both for small tensors.
+//
+// Every scale is fl32(max(amax, 1e-10) / 448) and every code
+// e4m3(fl32(x / scale)); "[vLLM] FP8" page, sections "스케일링 전략 체계"
+// and "블록 양자화", with the rounding readings stated in fp8w8a8.h.
+#include "common.cuh"
+#include "launch.h"
+
+namespace fp8k {
+namespace {
+
+// ------------------------------------------------ 1 x 128 activation groups --
+
+constexpr int kActThreads = 256;
+constexpr int kActUnroll = 4;                       // groups per half-warp
+constexpr int kActGroupsPerBlock = (kActThreads / 16) * kActUnroll;
+
+// Item i = g * M + m (m fastest): row m, K-group g. Half-warp h of the block
+// takes items base + u * 16 + h for u < kActUnroll.
+__global__ void __launch_bounds__(kActThreads) quant_act_group_kernel(const uint16_t *__restrict__ x,
+                                                                      uint8_t *__restrict__ q,
+                                                                      float *__restrict__ s, int64_t M,
+                                                                      int64_t K) {
+    const int64_t items = M * (K / 128);
+    const int hw = threadIdx.x >> 4;
+    const int hl = threadIdx.x & 15;
+    const int64_t base = static_cast<int64_t>(blockIdx.x) * kActGroupsPerBlock;
+
+    uint4 v[kActUnroll];
+    int64_t off[kActUnroll];
+#pragma unroll
+    for (int u = 0; u < kActUnroll; ++u) {
+        const int64_t it = base + u * 16 + hw;
+        v[u] = make_uint4(0u, 0u, 0u, 0u);
+        off[u] = -1;
+        if (it < items) {
+            const int64_t g = it / M, m = it - g * M;
+            off[u] = m * K + g * 128 + hl * 8;
+            v[u] = ld_stream_v4(x + off[u]);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < kActUnroll; ++u) {
+        float a = amax8(v[u]);
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 8));
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+        if (off[u] >= 0) {
+            const float sc = block_scale(a);
+            *reinterpret_cast<uint2 *>(q + off[u]) = quant8(v[u], sc);
+            if (hl == 0) s[base + u * 16 + hw] = sc;  // s[g * M + m] == s[item]
+        }
+    }
+}
+
+// --------------------------------------------------- 128 x 128 weight blocks --
+
+constexpr int kWThreads = 256;
+constexpr int kWChunks = 128 * 16 / kWThreads;  // 16-byte chunks per thread (8)
+
+// Block (nb, kb) = (blockIdx.y, blockIdx.x). Chunk c = t + 256 j covers row
+// c / 16 of the block and bytes 16 (c % 16) .. of the row's 256-byte span.
+__global__ void __launch_bounds__(kWThreads) quant_weight_block_kernel(const uint16_t *__restrict__ w,
+                                                                       uint8_t *__restrict__ q,
+                                                                       float *__restrict__ s, int64_t N,
+                                                                       int64_t K) {
+    __shared__ float warp_amax[kWThreads / 32];
+    const int t = threadIdx.x;
+    const int64_t kb = blockIdx.x, nb = blockIdx.y, Kg = K / 128;
+    const int col = (t & 15) * 8;
+    uint4 v[kWChunks];
+    float a = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kWChunks; ++j) {
+        const int64_t row = nb * 128 + (t >> 4) + 16 * j;
+        v[j] = make_uint4(0u, 0u, 0u, 0u);
+        if (row < N) v[j] = ld_stream_v4(w + row * K + kb * 128 + col);
+    }
+#pragma unroll
+    for (int j = 0; j < kWChunks; ++j) a = fmaxf(a, amax8(v[j]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    if ((t & 31) == 0) warp_amax[t >> 5] = a;
+    __syncthreads();
+    a = warp_amax[0];
+#pragma unroll
+    for (int i = 1; i < kWThreads / 32; ++i) a = fmaxf(a, warp_amax[i]);
+    const float sc = block_scale(a);
+#pragma unroll
+    for (int j = 0; j < kWChunks; ++j) {
+        const int64_t row = nb * 128 + (t >> 4) + 16 * j;
+        if (row < N) *reinterpret_cast<uint2 *>(q + row * K + kb * 128 + col) = quant8(v[j], sc);
+    }
+    if (t == 0) s[nb * Kg + kb] = sc;
+}
+
+// ------------------------------------------------------------- per tensor --
+
+constexpr int kTThreads = 256;
+constexpr int kTUnroll = 4;
+// Tensors up to this many elements take the single-CTA path.
+constexpr int64_t kSmallTensor = 1 << 17;
+
+__device__ __forceinline__ float block_reduce_max(float a, float *scratch) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = a;
+    __syncthreads();
+    a = scratch[0];
+    for (int i = 1; i < static_cast<int>(blockDim.x >> 5); ++i) a = fmaxf(a, scratch[i]);
+    return a;
+}
+
+// amax of the whole tensor into *amax_bits (zeroed before): the bit pattern of
+// a non-negative float orders like the float, so atomicMax on it is a max.
+__global__ void __launch_bounds__(kTThreads) tensor_amax_kernel(const uint16_t *__restrict__ x, int64_t n8,
+                                                                unsigned *__restrict__ amax_bits) {
+    __shared__ float scratch[kTThreads / 32];
+    float a = 0.0f;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kTThreads;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kTThreads + threadIdx.x; i < n8; i += stride * kTUnroll) {
+        uint4 v[kTUnroll];
+#pragma unroll
+        for (int u = 0; u < kTUnroll; ++u) {
+            const int64_t j = i + u * stride;
+            v[u] = j < n8 ? ld_stream_v4(x + j * 8) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < kTUnroll; ++u) a = fmaxf(a, amax8(v[u]));
+    }
+    a = block_reduce_max(a, scratch);
+    if (threadIdx.x == 0) atomicMax(amax_bits, __float_as_uint(a));
+}
+
+// Quantize with the scale from the amax in *amax_bits (dynamic) or the scale
+// in *scale (static).
+__global__ void __launch_bounds__(kTThreads) tensor_quant_kernel(const uint16_t *__restrict__ x,
+                                                                 uint8_t *__restrict__ q, int64_t n8,
+                                                                 const float *scale, int from_amax) {
+    const float stored = *scale;
+    const float sc = from_amax ? block_scale(stored) : stored;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kTThreads;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kTThreads + threadIdx.x; i < n8; i += stride * kTUnroll) {
+        uint4 v[kTUnroll];
+#pragma unroll
+        for (int u = 0; u < kTUnroll; ++u) {
+            const int64_t j = i + u * stride;
+            v[u] = j < n8 ? ld_stream_v4(x + j * 8) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < kTUnroll; ++u) {
+            const int64_t j = i + u * stride;
+            if (j < n8) *reinterpret_cast<uint2 *>(q + j * 8) = quant8(v[u], sc);
+        }
+    }
+}
+
+// *scale: amax bit pattern -> scale.
+__global__ void tensor_scale_finalize_kernel(float *scale) {
+    *scale = block_scale(*scale);
+}
+
+// Whole per-tensor quantization in one CTA (small tensors).
+__global__ void __launch_bounds__(1024) tensor_quant_small_kernel(const uint16_t *__restrict__ x,
+                                                                  uint8_t *__restrict__ q, int64_t n8,
+                                                                  float *scale, int is_static) {
+    __shared__ float scratch[32];
+    float sc;
+    if (is_static) {
+        sc = *scale;
+    } else {
+        float a = 0.0f;
+        for (int64_t i = threadIdx.x; i < n8; i += blockDim.x) a = fmaxf(a, amax8(ld_stream_v4(x + i * 8)));
+        sc = block_scale(block_reduce_max(a, scratch));
+    }
+    for (int64_t i = threadIdx.x; i < n8; i += blockDim.x)
+        *reinterpret_cast<uint2 *>(q + i * 8) = quant8(ld_stream_v4(x + i * 8), sc);
+    if (!is_static && threadIdx.x == 0) *scale = sc;
+}
+
+}  // namespace
+
+cudaError_t launch_quant_act_group(const void *x, void *q, float *s, int64_t M, int64_t K,
+                                   const DeviceInfo &dev, cudaStream_t stream) {
+    (void)dev;
+    const int64_t items = M * (K / 128);
+    const int64_t blocks = (items + kActGroupsPerBlock - 1) / kActGroupsPerBlock;
+    if (blocks == 0) return cudaSuccess;
+    if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    quant_act_group_kernel<<<static_cast<unsigned>(blocks), kActThreads, 0, stream>>>(
+        static_cast<const uint16_t *>(x), static_cast<uint8_t *>(q), s, M, K);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_weight_block(const void *w, void *q, float *s, int64_t N, int64_t K,
+                                      const DeviceInfo &dev, cudaStream_t stream) {
+    (void)dev;
+    const int64_t nb = (N + 127) / 128, kb = K / 128;
+    if (nb == 0 || kb == 0) return cudaSuccess;
+    if (nb > 65535 || kb > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    dim3 grid(static_cast<unsigned>(kb), static_cast<unsigned>(nb));
+    quant_weight_block_kernel<<<grid, kWThreads, 0, stream>>>(static_cast<const uint16_t *>(w),
+                                                              static_cast<uint8_t *>(q), s, N, K);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_per_tensor(const void *x, void *q, float *scale, int64_t n, bool is_static,
+                                    const DeviceInfo &dev, cudaStream_t stream) {
+    const int64_t n8 = n / 8;  // n is a multiple of 16
+    const uint16_t *xp = static_cast<const uint16_t *>(x);
+    uint8_t *qp = static_cast<uint8_t *>(q);
+    if (n8 == 0) {
+        if (is_static) return cudaSuccess;
+        tensor_quant_small_kernel<<<1, 32, 0, stream>>>(xp, qp, 0, scale, 0);
+        return cudaGetLastError();
+    }
+    if (n <= kSmallTensor) {
+        tensor_quant_small_kernel<<<1, 1024, 0, stream>>>(xp, qp, n8, scale, is_static ? 1 : 0);
+        return cudaGetLastError();
+    }
+    const int64_t want = (n8 + kTThreads * kTUnroll - 1) / (kTThreads * kTUnroll);
+    const int64_t cap = static_cast<int64_t>(dev.sm_count) * 8;
+    const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
+    if (!is_static) {
+        cudaError_t e = cudaMemsetAsync(scale, 0, sizeof(float), stream);
+        if (e != cudaSuccess) return e;
+        tensor_amax_kernel<<<grid, kTThreads, 0, stream>>>(xp, n8, reinterpret_cast<unsigned *>(scale));
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    tensor_quant_kernel<<<grid, kTThreads, 0, stream>>>(xp, qp, n8, scale, is_static ? 0 : 1);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || is_static) return e;
+    tensor_scale_finalize_kernel<<<1, 1, 0, stream>>>(scale);
+    return cudaGetLastError();
+}
+
+}  // namespace fp8k

@@ -1,0 +1,173 @@
+/*
+ * fp8w8a8.h — C ABI of the GB300 (sm_103a) FP8 W8A8 linear-layer library.
+ *
+ * What the library computes (readings of the pages are marked as such):
+ *
+ *  - E4M3: 4 exponent bits, 3 mantissa bits, no infinity, range +-448
+ *    ("[vLLM] FP8: 8비트 부동소수점 양자화", section "논문 핵심 내용" and its
+ *    format table). Reading: bias 7, S.1111.111 is NaN, encoding rounds to
+ *    nearest even and saturates to +-448, the sign of zero is kept.
+ *  - Symmetric scales, dynamic per-token 128-groups for activations and
+ *    static 128x128 blocks for weights; per-tensor scales, static or dynamic
+ *    (same page, sections "스케일링 전략 체계" and "블록 양자화"; the online
+ *    per-tensor mode of "서빙을 위한 양자화 가이드 FP8, AWQ, GPTQ", section
+ *    "연산까지 빨라지는 W8A8, FP8").
+ *    Reading: scale = fl32(max(amax, 1e-10) / 448) in IEEE FP32, code =
+ *    e4m3(fl32(x / scale)) with a correctly rounded FP32 division.
+ *  - GEMM on FP8 operands with high-precision accumulation, not a dequantize
+ *    to BF16 followed by a BF16 GEMM ("FP8 and FP4: Throughput Needs Scaling",
+ *    section "Kernel caveat가 마지막 관문이다"). Reading: FP32 accumulation
+ *    on the tensor cores within each 128-wide K block, the block's activation
+ *    and weight scales applied once per block in FP32, BF16 output.
+ *  - Matrix dimensions multiples of 16 for the FP8 tensor-core path ("FP8
+ *    serving slower than BF16", section "하드웨어 세대가 전제를 바꾼다").
+ *
+ * Conventions for every entry point:
+ *  - All matrices are dense and row-major. Every data pointer is caller-owned
+ *    DEVICE memory on the current CUDA device (BF16 as 2-byte values, E4M3 as
+ *    1-byte codes, scales as FP32); data pointers must be 16-byte aligned,
+ *    scale pointers 4-byte aligned. The library never allocates, frees or
+ *    synchronises inside a call.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream). Work is enqueued asynchronously on it; outputs are valid once
+ *    the stream reaches that point.
+ *  - The return value is a status (FP8_OK = 0). Argument errors are detected
+ *    on the host before anything is enqueued. A zero M (or rows) is a valid
+ *    no-op.
+ *  - Device-side waits in the kernels are bounded (about one second); if one
+ *    expires the kernel stops early and records FP8_ERR_TIMEOUT, which
+ *    fp8_device_error() reports. Kernels never trap.
+ */
+#ifndef FP8W8A8_H
+#define FP8W8A8_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum fp8_status {
+    FP8_OK = 0,
+    FP8_ERR_NULL = 1,        /* a required pointer is NULL */
+    FP8_ERR_SHAPE = 2,       /* negative size, K == 0, or a size that breaks a multiple-of rule */
+    FP8_ERR_ALIGN = 3,       /* data pointer not 16-byte aligned, scale pointer not 4-byte aligned */
+    FP8_ERR_UNSUPPORTED = 4, /* group/block size other than 128, or too many groups */
+    FP8_ERR_ARG = 5,         /* other invalid argument (num_groups, group_offsets) */
+    FP8_ERR_DEVICE = 6,      /* current device is not compute capability 10.3 (sm_103a) */
+    FP8_ERR_CUDA = 7,        /* a CUDA runtime call or kernel launch failed */
+    FP8_ERR_TIMEOUT = 8      /* a bounded device-side wait expired (reported by fp8_device_error) */
+};
+
+/* Width of an activation group along K and the side of a weight block. */
+#define FP8_GROUP 128
+/* Largest num_groups accepted by fp8_block_gemm. */
+#define FP8_MAX_GROUPS 256
+
+/*
+ * Dynamic activation quantization, one scale per token per 128-wide K group
+ * (the "128 block dynamic symmetric" strategy, kFp8Dynamic128Sym, of the vLLM
+ * page's section "스케일링 전략 체계"; reading: 1 x 128 groups along K).
+ *
+ *   x_bf16  [M][K] BF16, input.
+ *   q_e4m3  [M][K] E4M3 codes, output.
+ *   scales  [K/128][M] FP32, output: scales[g*M + m] belongs to row m, columns
+ *           128g .. 128g+127 (M contiguous, so a GEMM tile reads a run of rows).
+ *   group_k must be 128. K must be a positive multiple of 128; M >= 0 is any.
+ * Errors: NULL, SHAPE, ALIGN, UNSUPPORTED, DEVICE, CUDA.
+ */
+int fp8_quant_act_group(const void *x_bf16, void *q_e4m3, float *scales,
+                        int64_t M, int64_t K, int group_k, void *stream);
+
+/*
+ * Weight block quantization (offline, at load time), one scale per 128 x 128
+ * block (weight_block_size of section "블록 양자화"; kFp8Static128BlockSym).
+ *
+ *   w_bf16  [N][K] BF16, input.
+ *   q_e4m3  [N][K] E4M3 codes, output.
+ *   scales  [ceil(N/128)][K/128] FP32, output (row-major). The last block row
+ *           may be short when N is not a multiple of 128.
+ *   block_n and block_k must be 128; K a positive multiple of 128; N >= 0.
+ * Errors: NULL, SHAPE, ALIGN, UNSUPPORTED, DEVICE, CUDA.
+ */
+int fp8_quant_weight_block(const void *w_bf16, void *q_e4m3, float *scales,
+                           int64_t N, int64_t K, int block_n, int block_k, void *stream);
+
+/*
+ * Per-tensor quantization (kFp8StaticTensorSym / kFp8DynamicTensorSym; the
+ * online "--quantization fp8" mode that keeps one scale per tensor and
+ * recomputes the activation scale every step).
+ *
+ *   x_bf16  [rows][cols] BF16, input.
+ *   q_e4m3  [rows][cols] E4M3 codes, output.
+ *   scale   ONE FP32 in device memory. is_static != 0: input, must hold a
+ *           finite positive scale. is_static == 0: output, receives
+ *           fl32(max(amax, 1e-10) / 448) of the whole tensor.
+ *   cols must be a positive multiple of 16; rows >= 0.
+ * A dynamic call enqueues up to four launches (zero the slot, amax, quantize,
+ * write the scale); the scale slot holds the amax bit pattern in between, so
+ * it must not be read by other work until the call's work is done.
+ * Errors: NULL, SHAPE, ALIGN, DEVICE, CUDA.
+ */
+int fp8_quant_per_tensor(const void *x_bf16, void *q_e4m3, float *scale,
+                         int64_t rows, int64_t cols, int is_static, void *stream);
+
+/*
+ * Block-scaled FP8 GEMM, Y = A * W^T with 1x128 activation groups and 128x128
+ * weight blocks:
+ *   Y[m,n] = bf16( sum_g Sa[g][m] * Sw[n/128][g] * sum_{k in g} dec(Qa[m,k]) dec(Qw[n,k]) )
+ * The inner sums run on the tensor cores in FP32; each 128-wide K block is
+ * scaled and added to an FP32 accumulator once.
+ *
+ *   qa   [M][K] E4M3, sa [K/128][M] FP32 (as written by fp8_quant_act_group).
+ *   qw   [N][K] E4M3, sw [ceil(N/128)][K/128] FP32 (as written by
+ *        fp8_quant_weight_block). Grouped: qw [num_groups][N][K] and
+ *        sw [num_groups][ceil(N/128)][K/128], expert e at offset e*N*K / e*ceil(N/128)*(K/128).
+ *   y    [M][N] BF16, output.
+ *   block_n, block_k, group_k must be 128. K a positive multiple of 128,
+ *   N a positive multiple of 16, M >= 0.
+ *   num_groups == 1 and group_offsets == NULL: dense GEMM.
+ *   Otherwise grouped (mixture-of-experts): group_offsets is DEVICE int32
+ *   [num_groups+1], non-decreasing, with 0 <= offsets[0] and
+ *   offsets[num_groups] <= M; rows [offsets[e], offsets[e+1]) of qa/y use
+ *   expert e's weights. Rows outside [offsets[0], offsets[num_groups]) are not
+ *   written. Offsets are read on the device and are trusted.
+ *   num_groups in [1, FP8_MAX_GROUPS].
+ * M <= 16 (dense) uses the weight-streaming decode kernel, otherwise the
+ * tile-persistent prefill kernel.
+ * Errors: NULL, SHAPE, ALIGN, UNSUPPORTED, ARG, DEVICE, CUDA.
+ */
+int fp8_block_gemm(const void *qa, const float *sa, const void *qw, const float *sw,
+                   void *y_bf16, int64_t M, int64_t N, int64_t K,
+                   int block_n, int block_k, int group_k,
+                   int num_groups, const int32_t *group_offsets, void *stream);
+
+/*
+ * Per-tensor FP8 GEMM: Y[m,n] = bf16( sa * sw * sum_k dec(Qa[m,k]) dec(Qw[n,k]) ),
+ * FP32 accumulation over all of K, one scale product applied at the end.
+ *
+ *   qa [M][K] E4M3, qw [N][K] E4M3, y [M][N] BF16.
+ *   sa, sw: ONE FP32 each, in DEVICE memory (as written by fp8_quant_per_tensor).
+ *   K and N positive multiples of 16, M >= 0.
+ * Errors: NULL, SHAPE, ALIGN, DEVICE, CUDA.
+ */
+int fp8_tensor_gemm(const void *qa, const float *sa, const void *qw, const float *sw,
+                    void *y_bf16, int64_t M, int64_t N, int64_t K, void *stream);
+
+/* Static, NUL-terminated description of a status code. Never NULL. */
+const char *fp8_status_string(int status);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's error
+ * word, which kernels set when a bounded wait expires. *out_code receives
+ * FP8_OK or FP8_ERR_TIMEOUT; *out_site (may be NULL) a number naming the wait
+ * that expired. Returns FP8_OK, or FP8_ERR_CUDA if the synchronisation or the
+ * read failed (e.g. an earlier kernel faulted).
+ */
+int fp8_device_error(void *stream, int *out_code, int *out_site);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8W8A8_H */

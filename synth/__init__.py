@@ -181,3 +181,24 @@ def moe_case(tokens: int = 4096, experts: int = 8, N: int = 2048, K: int = 7168,
     token_of_row, offsets = route_top2(tokens, experts, seed)
     w = np.stack([weights(N, K, seed, f"moe/W{e}", sigma=0.02) for e in range(experts)])
     return np.ascontiguousarray(x[token_of_row]), w, offsets
+
+
+# ------------------------------------------------ device-side generation ---
+
+def device_normal_bf16(rows: int, cols: int, seed: int, label: str, sigma: float = 1.0,
+                       outlier_cols=None, outlier_rows=None, outlier_scale: float = 1.0, device="cuda"):
+    """Same distributions as `activations` / `weights`, drawn on the GPU with
+    torch's seeded Philox generator (for the large benchmark inputs, which no
+    oracle reads): N(0, sigma^2) rounded to BF16, the given columns or rows
+    multiplied by `outlier_scale` before rounding."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(stream_seed(seed, label) & 0x7FFFFFFFFFFFFFFF)
+    x = torch.randn((rows, cols), generator=g, device=device, dtype=torch.float32)
+    if sigma != 1.0:
+        x.mul_(sigma)
+    if outlier_cols is not None and len(outlier_cols):
+        x[:, torch.as_tensor(outlier_cols, device=device)] *= outlier_scale
+    if outlier_rows is not None and len(outlier_rows):
+        x[torch.as_tensor(outlier_rows, device=device), :] *= outlier_scale
+    return x.to(torch.bfloat16)
