@@ -521,6 +521,73 @@ def reference_arm(args):
     print(json.dumps(line))
 
 
+# ------------------------------------------------------------ single case --
+
+def run_case(spec: str, launches: int):
+    """One kernel on one shape, for profiling: KIND:M:N:K with KIND in
+    decode|prefill|tensor|moe|act|weight|ptensor. Prints per-launch times."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from fp8_w8a8_quantized_group_gb300 import ops
+    kind, M, N, K = spec.split(":")
+    M, N, K = int(M), int(N), int(K)
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(0)
+    x = synth.device_normal_bf16(M, K, 0, "case/X", device=dev)
+    if kind in ("decode", "prefill"):
+        qa, sa = ops.quant_act_group(x)
+        qw, sw = ops.quant_weight_block(synth.device_normal_bf16(N, K, 0, "case/W", sigma=0.02, device=dev))
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        fn = lambda: ops.fp8_block_gemm(qa, sa, qw, sw, y)  # noqa: E731
+    elif kind == "tensor":
+        qa, sa = ops.quant_per_tensor(x)
+        qw, sw = ops.quant_per_tensor(synth.device_normal_bf16(N, K, 0, "case/W", sigma=0.02, device=dev))
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        fn = lambda: ops.fp8_tensor_gemm(qa, sa, qw, sw, y)  # noqa: E731
+    elif kind == "moe":
+        E = 8
+        tok, off = synth.route_top2(M // 2, E, seed=0)
+        xp = x[: M // 2].index_select(0, torch.from_numpy(tok).to(dev))
+        qa, sa = ops.quant_act_group(xp)
+        qw = torch.empty((E, N, K), dtype=torch.uint8, device=dev)
+        sw = torch.empty((E, N // 128, K // 128), dtype=torch.float32, device=dev)
+        for e in range(E):
+            ops.fp8_quant_weight_block(synth.device_normal_bf16(N, K, 0, f"case/W{e}", sigma=0.02, device=dev),
+                                       qw[e], sw[e])
+        y = torch.empty((xp.shape[0], N), dtype=torch.bfloat16, device=dev)
+        offd = torch.from_numpy(off).to(dev)
+        fn = lambda: ops.fp8_block_gemm(qa, sa, qw, sw, y, num_groups=E, group_offsets=offd)  # noqa: E731
+    elif kind == "act":
+        qa = torch.empty((M, K), dtype=torch.uint8, device=dev)
+        sa = torch.empty((K // 128, M), dtype=torch.float32, device=dev)
+        fn = lambda: ops.fp8_quant_act_group(x, qa, sa)  # noqa: E731
+    elif kind == "weight":
+        qw = torch.empty((M, K), dtype=torch.uint8, device=dev)
+        sw = torch.empty((-(-M // 128), K // 128), dtype=torch.float32, device=dev)
+        fn = lambda: ops.fp8_quant_weight_block(x, qw, sw)  # noqa: E731
+    elif kind == "ptensor":
+        q = torch.empty((M, K), dtype=torch.uint8, device=dev)
+        s = torch.empty(1, dtype=torch.float32, device=dev)
+        fn = lambda: ops.fp8_quant_per_tensor(x, q, s, False)  # noqa: E731
+    else:
+        raise SystemExit(f"unknown case kind {kind}")
+    times = []
+    for _ in range(launches):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1) * 1e3)
+    code, site = ops.fp8_device_error()
+    print(json.dumps({"case": spec, "us": times, "device_error": code}))
+    if code:
+        raise SystemExit(1)
+
+
 # ------------------------------------------------------------------- main --
 
 def main():
@@ -531,7 +598,12 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--sections", default="prefill,tensor,moe,quant")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--case", default=None, help="profile one kernel: KIND:M:N:K")
+    ap.add_argument("--launches", type=int, default=3)
     args = ap.parse_args()
+    if args.case:
+        run_case(args.case, args.launches)
+        return
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":
         reference_arm(args)
