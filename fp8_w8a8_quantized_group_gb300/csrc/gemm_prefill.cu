@@ -9,23 +9,26 @@
 // dynamic 128-groups for activations ("[vLLM] FP8", section "블록 양자화").
 // The kernel below is this library's own design for GB300:
 //
-//  - one CTA per SM, persistent over output tiles of 128 x BN;
+//  - one CTA per SM, persistent over output tiles of 128 x BN (BN = 128/256);
 //  - warp 0 (one lane): TMA producer, fills a ring of shared-memory stages;
 //    one stage = one 128-wide K block of A (128 x 128 B) and B (BN x 128 B),
 //    both K-major with 128-byte swizzle;
-//  - warp 1 (one lane): issues 4 tcgen05.mma (K = 32 each) per stage into a
-//    fresh TMEM accumulator, so TMEM holds the FP32 partial of ONE K block;
-//    two TMEM buffers alternate so the MMA of block k+1 runs while block k
-//    is being promoted;
-//  - warps 4..7: epilogue, one thread per output row; per K block it loads
-//    the partial from TMEM and adds partial * (Sa * Sw) into FP32 registers
-//    (the per-block scale promotion), then writes BF16 at the end of the
-//    tile;
-//  - per-tensor mode: the MMAs accumulate all of K in TMEM and the single
-//    scale product is applied once per tile.
+//  - warp 1: owns TMEM; one lane issues 4 tcgen05.mma (K = 32 each) per stage
+//    into a fresh TMEM accumulator, so a TMEM buffer holds the FP32 partial of
+//    ONE K block; the 512 TMEM columns hold 512/BN such buffers, so the MMAs
+//    run up to that many K blocks ahead of the promotion;
+//  - warps 4..11 (two warpgroups): epilogue. Warp w reads TMEM lanes
+//    32*(w%4).. (the lane quarter the hardware gives that warp) and one half
+//    of the tile's columns; per K block each thread adds
+//    partial * (Sa[m] * Sw) for its row into FP32 registers (the per-block
+//    scale promotion) and, after the last K block, writes its half-row as BF16;
+//  - warpgroup 0 gives registers to the epilogue warpgroups (setmaxnreg);
+//  - per-tensor mode: the MMAs accumulate all of K in TMEM; the epilogue
+//    applies the single scale product once per tile, streaming TMEM to Y.
 //
 // Every wait is bounded (common.cuh); on expiry the CTA records an error,
-// stops issuing, lets the copies it issued land and frees its TMEM.
+// stops issuing, lets the copies and MMAs it issued finish and frees TMEM.
+#include <cstdlib>
 #include <mutex>
 
 #include "common.cuh"
@@ -36,8 +39,15 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 128;  // one K block: one stage, 4 MMAs of K = 32
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
+constexpr int kEpiThreads = 256;
 constexpr int kMaxGroups = 256;
+constexpr int kTmemCols = 512;
+// Register split: warpgroup 0 shrinks, the two epilogue warpgroups grow.
+// 128 * kRegsLow + 256 * kRegsHigh must not exceed 384 * (registers the
+// kernel is compiled with); the launcher checks that before every launch.
+constexpr int kRegsLow = 80;
+constexpr int kRegsHigh = 200;
 
 // Bounded-wait sites reported through the error word.
 enum : unsigned { kSiteProdEmpty = 101, kSiteMmaTmem = 102, kSiteMmaFull = 103, kSiteEpiFull = 104,
@@ -45,12 +55,14 @@ enum : unsigned { kSiteProdEmpty = 101, kSiteMmaTmem = 102, kSiteMmaFull = 103, 
 
 template <int BN>
 struct Cfg {
-    static constexpr int kStages = 6;
+    static constexpr int kStages = BN == 128 ? 6 : 4;
     static constexpr int kABytes = BM * BK;
     static constexpr int kBBytes = BN * BK;
     static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kTmemCols = 2 * BN;
-    static constexpr int kBarrierBytes = 8 * (2 * kStages + 4) + 16;
+    static constexpr int kBufs = kTmemCols / BN;        // TMEM partial buffers
+    static constexpr int kCols = BN / 2;                // columns per epilogue thread
+    static constexpr int kChunk = BN == 128 ? 64 : 32;  // TMEM columns loaded per wait
+    static constexpr int kBarrierBytes = 8 * (2 * kStages + 2 * kBufs) + 16;
     static constexpr int kTableBytes = 4 * (3 * kMaxGroups + 2);
     static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarrierBytes + kTableBytes;
 };
@@ -91,6 +103,22 @@ struct Sched {
     }
 };
 
+template <int CH>
+__device__ __forceinline__ void tmem_ld_chunk(uint32_t taddr, float (&p)[CH]);
+template <>
+__device__ __forceinline__ void tmem_ld_chunk<64>(uint32_t taddr, float (&p)[64]) { tmem_ld64(taddr, p); }
+template <>
+__device__ __forceinline__ void tmem_ld_chunk<32>(uint32_t taddr, float (&p)[32]) { tmem_ld32(taddr, p); }
+
+__device__ __forceinline__ uint4 pack8_scaled(const float *p, float s) {
+    uint4 v;
+    v.x = pack_bf16x2(p[0] * s, p[1] * s);
+    v.y = pack_bf16x2(p[2] * s, p[3] * s);
+    v.z = pack_bf16x2(p[4] * s, p[5] * s);
+    v.w = pack_bf16x2(p[6] * s, p[7] * s);
+    return v;
+}
+
 template <int BN, bool PER_TENSOR>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -105,8 +133,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *full = reinterpret_cast<uint64_t *>(sB + C::kStages * C::kBBytes);
     uint64_t *empty = full + C::kStages;
     uint64_t *tfull = empty + C::kStages;
-    uint64_t *tempty = tfull + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
+    uint64_t *tempty = tfull + C::kBufs;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + C::kBufs);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     int *t_lo = reinterpret_cast<int *>(tmem_slot + 4);
     int *t_hi = t_lo + kMaxGroups;
@@ -119,7 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
-        for (int b = 0; b < 2; ++b) { mbar_init(&tfull[b], 1); mbar_init(&tempty[b], 128); }
+        for (int b = 0; b < C::kBufs; ++b) { mbar_init(&tfull[b], 1); mbar_init(&tempty[b], kEpiThreads); }
         *abort_flag = 0;
         fence_barrier_init();
         if (offsets != nullptr) {
@@ -139,7 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     if (warp == 0 && lane == 0) { tma_prefetch_desc(&tmA); tma_prefetch_desc(&tmB); }
-    if (warp == 2) { tmem_alloc(tmem_slot, C::kTmemCols); tmem_relinquish(); }
+    if (warp == 1) { tmem_alloc(tmem_slot, kTmemCols); tmem_relinquish(); }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -151,8 +179,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     sched.lo = t_lo; sched.hi = t_hi; sched.start = t_start;
     const int total = offsets != nullptr ? t_start[groups] : sched.num_m * num_n;
 
-    if (warp == 0) {
-        if (lane == 0) {
+    if (warp < 4) {
+        regs_shrink<kRegsLow>();
+        if (warp == 0 && lane == 0) {
             // ------------------------------------------------ TMA producer --
             uint32_t stage = 0, phase = 0;
             int issued = 0;
@@ -177,9 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (global_ns() - t0 > kWaitLimitNs) { record_error(err, kErrTimeout, kSiteDrain); break; }
                 }
             }
-        }
-    } else if (warp == 1) {
-        if (lane == 0) {
+        } else if (warp == 1 && lane == 0) {
             // ------------------------------------------------- MMA issuer --
             constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
             uint32_t stage = 0, phase = 0, buf = 0, bphase = 0;
@@ -209,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     last_phase = phase;
                     if (!PER_TENSOR || kb == Kg - 1) {
                         umma_commit(&tfull[buf]);
-                        if (++buf == 2) { buf = 0; bphase ^= 1u; }
+                        if (++buf == C::kBufs) { buf = 0; bphase ^= 1u; }
                     }
                     if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
                 }
@@ -224,11 +251,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-    } else if (warp >= 4) {
+        __syncwarp();  // lanes 1..31 wait for their lane 0
+    } else {
+        regs_grow<kRegsHigh>();
         // ------------------------------------------------------ epilogue --
-        const int ep = warp - 4;
-        const int r = ep * 32 + lane;
-        const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(ep * 32) << 16);
+        const int quarter = warp & 3;      // TMEM lane quarter this warp may access
+        const int half = (warp - 4) >> 2;  // which half of the tile's columns
+        const int r = quarter * 32 + lane; // row within the tile
+        const int c0 = half * C::kCols;    // first column within the tile
+        const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + c0;
         uint32_t buf = 0, bphase = 0;
         float tensor_scale = 0.0f;
         if (PER_TENSOR) tensor_scale = sa[0] * sw[0];
@@ -237,73 +268,78 @@ __global__ void __launch_bounds__(kThreads, 1)
             const Tile tl = sched.get(t);
             const int m = tl.m0 + r;
             const bool row_in = m < M;
-            float acc[BN];
-#pragma unroll
-            for (int j = 0; j < BN; ++j) acc[j] = 0.0f;
+            const bool row_out = row_in && m < tl.row_end;
+            __nv_bfloat16 *yrow = y + static_cast<int64_t>(m) * N + tl.n0 + c0;
             if (!PER_TENSOR) {
-                const float *swg = sw + static_cast<int64_t>(tl.group) * Nb * Kg;
-                const int nb0 = tl.n0 / 128;
-                for (int kb = 0; kb < Kg; ++kb) {
-                    // scales for this K block (loads issued before the wait)
-                    const float sa_v = row_in ? __ldg(sa + static_cast<int64_t>(kb) * M + m) : 0.0f;
-                    float sw_v[(BN + 127) / 128];
+                float acc[C::kCols];
 #pragma unroll
-                    for (int j = 0; j < (BN + 127) / 128; ++j)
-                        sw_v[j] = (nb0 + j < Nb) ? __ldg(swg + static_cast<int64_t>(nb0 + j) * Kg + kb) : 0.0f;
+                for (int j = 0; j < C::kCols; ++j) acc[j] = 0.0f;
+                const int nb = (tl.n0 + c0) / 128;  // this half lies in one 128-column weight block
+                const float *swp = sw + (static_cast<int64_t>(tl.group) * Nb + (nb < Nb ? nb : Nb - 1)) * Kg;
+                const float *sap = sa + m;
+                float sa_next = row_in ? __ldg(sap) : 0.0f;
+                float sw_next = __ldg(swp);
+                for (int kb = 0; kb < Kg; ++kb) {
+                    const float sc = sa_next * sw_next;
+                    if (kb + 1 < Kg) {  // next block's scales, in flight during this block
+                        sa_next = row_in ? __ldg(sap + static_cast<int64_t>(kb + 1) * M) : 0.0f;
+                        sw_next = __ldg(swp + kb + 1);
+                    }
                     ok = __all_sync(0xffffffffu, mbar_wait(&tfull[buf], bphase, abort_flag, err, kSiteEpiFull));
                     if (!ok) break;
                     tc_fence_after();
 #pragma unroll
-                    for (int c = 0; c < BN / 32; ++c) {
-                        float p[32];
-                        tmem_ld32(lane_addr + buf * BN + c * 32, p);
-                        const float sc = sa_v * sw_v[(c * 32) / 128];
+                    for (int c = 0; c < C::kCols / C::kChunk; ++c) {
+                        float p[C::kChunk];
+                        tmem_ld_chunk<C::kChunk>(lane_addr + buf * BN + c * C::kChunk, p);
+                        if (c == C::kCols / C::kChunk - 1) {  // all of this buffer is in registers
+                            tc_fence_before();
+                            mbar_arrive(&tempty[buf]);
+                        }
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) acc[c * 32 + j] = fmaf(p[j], sc, acc[c * 32 + j]);
+                        for (int j = 0; j < C::kChunk; ++j)
+                            acc[c * C::kChunk + j] = fmaf(p[j], sc, acc[c * C::kChunk + j]);
                     }
-                    tc_fence_before();
-                    mbar_arrive(&tempty[buf]);
-                    if (++buf == 2) { buf = 0; bphase ^= 1u; }
+                    if (++buf == C::kBufs) { buf = 0; bphase ^= 1u; }
+                }
+                if (!ok) break;
+                if (row_out) {
+#pragma unroll
+                    for (int c = 0; c < C::kCols / 8; ++c)
+                        if (tl.n0 + c0 + c * 8 < N)
+                            *reinterpret_cast<uint4 *>(yrow + c * 8) = pack8_scaled(acc + c * 8, 1.0f);
                 }
             } else {
                 ok = __all_sync(0xffffffffu, mbar_wait(&tfull[buf], bphase, abort_flag, err, kSiteEpiFull));
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
-                for (int c = 0; c < BN / 32; ++c) {
-                    float p[32];
-                    tmem_ld32(lane_addr + buf * BN + c * 32, p);
+                for (int c = 0; c < C::kCols / C::kChunk; ++c) {
+                    float p[C::kChunk];
+                    tmem_ld_chunk<C::kChunk>(lane_addr + buf * BN + c * C::kChunk, p);
+                    if (c == C::kCols / C::kChunk - 1) {
+                        tc_fence_before();
+                        mbar_arrive(&tempty[buf]);
+                    }
+                    if (row_out) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) acc[c * 32 + j] = p[j] * tensor_scale;
-                }
-                tc_fence_before();
-                mbar_arrive(&tempty[buf]);
-                if (++buf == 2) { buf = 0; bphase ^= 1u; }
-            }
-            if (!ok) break;
-            if (m < tl.row_end && row_in) {
-                __nv_bfloat16 *yrow = y + static_cast<int64_t>(m) * N + tl.n0;
-#pragma unroll
-                for (int c = 0; c < BN / 8; ++c) {
-                    if (tl.n0 + c * 8 < N) {
-                        uint4 v;
-                        v.x = pack_bf16x2(acc[c * 8 + 0], acc[c * 8 + 1]);
-                        v.y = pack_bf16x2(acc[c * 8 + 2], acc[c * 8 + 3]);
-                        v.z = pack_bf16x2(acc[c * 8 + 4], acc[c * 8 + 5]);
-                        v.w = pack_bf16x2(acc[c * 8 + 6], acc[c * 8 + 7]);
-                        *reinterpret_cast<uint4 *>(yrow + c * 8) = v;
+                        for (int q = 0; q < C::kChunk / 8; ++q) {
+                            const int col = c * C::kChunk + q * 8;
+                            if (tl.n0 + c0 + col < N)
+                                *reinterpret_cast<uint4 *>(yrow + col) = pack8_scaled(p + q * 8, tensor_scale);
+                        }
                     }
                 }
+                if (++buf == C::kBufs) { buf = 0; bphase ^= 1u; }
             }
         }
     }
 
-    __syncwarp();  // lanes 1..31 of the producer and MMA warps wait for lane 0
     tc_fence_before();
     __syncthreads();
-    if (warp == 2) {
+    if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, C::kTmemCols);
+        tmem_dealloc(tmem_base, kTmemCols);
     }
 }
 
@@ -317,8 +353,15 @@ cudaError_t launch_variant(const void *qa, const float *sa, const void *qw, cons
     int device = 0;
     cudaGetDevice(&device);
     std::call_once(attr_once[device & 63], [&] {
-        attr_err[device & 63] = cudaFuncSetAttribute(gemm_prefill_kernel<BN, PER_TENSOR>,
-                                                     cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(gemm_prefill_kernel<BN, PER_TENSOR>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        // The register re-split inside the kernel needs the launch to hold at
+        // least 128 * kRegsLow + 256 * kRegsHigh registers; refuse otherwise.
+        cudaFuncAttributes fa;
+        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, gemm_prefill_kernel<BN, PER_TENSOR>);
+        if (e == cudaSuccess && fa.numRegs * kThreads < 128 * kRegsLow + 256 * kRegsHigh)
+            e = cudaErrorInvalidConfiguration;
+        attr_err[device & 63] = e;
     });
     if (attr_err[device & 63] != cudaSuccess) return attr_err[device & 63];
 
@@ -342,13 +385,28 @@ cudaError_t launch_variant(const void *qa, const float *sa, const void *qw, cons
     return cudaGetLastError();
 }
 
+// Tile width: FP8_PREFILL_BN=128|256 overrides the default (256 when N is a
+// multiple of 256, else 128).
+int pick_bn(int64_t N) {
+    static const int forced = [] {
+        const char *v = std::getenv("FP8_PREFILL_BN");
+        return v ? std::atoi(v) : 0;
+    }();
+    if (forced == 128 || forced == 256) return forced;
+    return (N % 256 == 0) ? 256 : 128;
+}
+
 }  // namespace
 
 cudaError_t launch_gemm_prefill(const void *qa, const float *sa, const void *qw, const float *sw, void *y,
                                 int64_t M, int64_t N, int64_t K, int num_groups, const int32_t *offsets,
                                 bool per_tensor, const DeviceInfo &dev, cudaStream_t stream) {
-    if (per_tensor)
+    const int bn = pick_bn(N);
+    if (per_tensor) {
+        if (bn == 256) return launch_variant<256, true>(qa, sa, qw, sw, y, M, N, K, num_groups, offsets, dev, stream);
         return launch_variant<128, true>(qa, sa, qw, sw, y, M, N, K, num_groups, offsets, dev, stream);
+    }
+    if (bn == 256) return launch_variant<256, false>(qa, sa, qw, sw, y, M, N, K, num_groups, offsets, dev, stream);
     return launch_variant<128, false>(qa, sa, qw, sw, y, M, N, K, num_groups, offsets, dev, stream);
 }
 
