@@ -178,6 +178,23 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
     return p;
 }
 
+// Warm L2 with one tile of a tensor map (no shared memory written, nothing
+// to wait for).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(x), "r"(y)
+                 : "memory");
+}
+
+// ------------------------------------------------ programmatic dependent launch --
+
+// Wait until the grids this one depends on have completed and their memory
+// is visible (no-op when the launch was not programmatic).
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allow the next grid in the stream to be scheduled; it still waits for this
+// grid's completion in its own grid_dep_wait().
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- tcgen05 --
 
 // Allocate `ncols` TMEM columns (power of two >= 32); the whole warp calls.
@@ -293,6 +310,30 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&r)[64]) {
     for (int i = 0; i < 64; ++i) r[i] = __uint_as_float(u[i]);
 }
 
+// Issue a 16-column TMEM load without waiting; the registers are valid only
+// after tmem_wait16() on the same array.
+__device__ __forceinline__ void tmem_ld16_async(uint32_t taddr, uint32_t (&u)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7]),
+          "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]), "=r"(u[13]), "=r"(u[14]),
+          "=r"(u[15])
+        : "r"(taddr)
+        : "memory");
+}
+
+// Wait for this thread's outstanding TMEM loads. The registers of `u` are
+// passed through the wait so that no use of them is scheduled before it.
+__device__ __forceinline__ void tmem_wait16(uint32_t (&u)[16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(u[0]), "+r"(u[1]), "+r"(u[2]), "+r"(u[3]), "+r"(u[4]), "+r"(u[5]), "+r"(u[6]),
+                   "+r"(u[7]), "+r"(u[8]), "+r"(u[9]), "+r"(u[10]), "+r"(u[11]), "+r"(u[12]), "+r"(u[13]),
+                   "+r"(u[14]), "+r"(u[15])
+                 :
+                 : "memory");
+}
+
 // Warpgroup register re-split (all 128 threads of the warpgroup execute it).
 template <int N>
 __device__ __forceinline__ void regs_shrink() {
@@ -338,9 +379,11 @@ __device__ __forceinline__ uint32_t map_shared_rank(uint32_t saddr, uint32_t ran
     return r;
 }
 
+// Load from distributed shared memory. No memory clobber, so that several
+// of these issue back to back; order them after a cluster barrier.
 __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
     float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
     return v;
 }
 

@@ -12,11 +12,17 @@
 //  - weights stream through a ring of TMA stages (16 KB of weights + 2 KB
 //    of activation codes per 128-wide K block), one lane issuing, so many
 //    bytes are in flight per SM with no register staging;
-//  - K is split across the CTAs of a thread-block cluster (up to 8) to put
-//    enough CTAs on the GPU; each CTA promotes its K blocks with the scales
-//    in FP32 registers, and the partial sums are reduced through distributed
-//    shared memory, each CTA of the cluster summing and storing a slice of
-//    the 128 rows. No global scratch memory is used.
+//  - K is split across the CTAs of a thread-block cluster (up to 8) so that
+//    all CTAs of the grid are resident at once (one wave); each CTA promotes
+//    its K blocks with the scales in FP32 registers, and the partial sums are
+//    reduced through distributed shared memory, each CTA of the cluster
+//    summing (in a fixed order) and storing a slice of the 128 rows. No
+//    global scratch memory is used;
+//  - launched as a programmatic dependent of the previous kernel in the
+//    stream: before that kernel is known to be complete the CTA only warms
+//    L2 with its first weight tiles (L2 is coherent, so this is safe even if
+//    the previous kernel writes the weights); every shared-memory load and
+//    every global write comes after griddepcontrol.wait.
 //
 // Block mode applies Sw[n/128][kb] * Sa[kb][m] per K block; per-tensor mode
 // accumulates all of the CTA's K range in TMEM and applies sa * sw once.
@@ -37,6 +43,7 @@ constexpr int kXBytes = kTok * BK;
 constexpr int kThreads = 256;
 constexpr int kTmemCols = 32;   // two 16-column partial buffers
 constexpr int kRedStride = kTok + 1;
+constexpr int kL2Warm = 8;      // weight tiles warmed in L2 before the upstream grid completes
 constexpr int kSmemBytes = 1024 + kStages * (kWBytes + kXBytes) + 8 * (2 * kStages + 4) + 16;
 
 enum : unsigned { kSiteProdEmpty = 201, kSiteMmaTmem = 202, kSiteMmaFull = 203, kSiteEpiFull = 204,
@@ -83,10 +90,14 @@ __global__ void __launch_bounds__(kThreads, 2)
     float acc[kTok];
 #pragma unroll
     for (int j = 0; j < kTok; ++j) acc[j] = 0.0f;
+    grid_dep_launch();
 
     if (warp == 0) {
         if (lane == 0) {
             // -------------------------------------------------- producer --
+            const int warm = (kb1 - kb0) < kL2Warm ? (kb1 - kb0) : kL2Warm;
+            for (int i = 0; i < warm; ++i) tma_prefetch_l2_2d(&tmW, (kb0 + i) * BK, n0);
+            grid_dep_wait();
             const uint64_t stream_once = policy_evict_first();
             uint32_t stage = 0, phase = 0;
             int issued = 0;
@@ -108,6 +119,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
         }
     } else if (warp == 1) {
+        grid_dep_wait();
         if (lane == 0) {
             // ------------------------------------------------------- MMA --
             constexpr uint32_t idesc = idesc_e4m3_f32(kRows, kTok);
@@ -152,6 +164,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int r = ep * 32 + lane;  // weight row within the CTA's 128
         const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(ep * 32) << 16);
         uint32_t buf = 0, bphase = 0;
+        grid_dep_wait();
         if (!PER_TENSOR) {
             const float *swrow = sw + static_cast<int64_t>(nb) * Kg;
             for (int kb = kb0; kb < kb1; ++kb) {
@@ -191,6 +204,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 
     __syncwarp();  // lanes 1..31 of the producer and MMA warps wait for lane 0
+    grid_dep_wait();  // every thread below may write Y
 
     if (splits > 1) {
         // ------------------------------------- cluster split-K reduction --
@@ -212,8 +226,13 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int j = idx / rows_per;
             const int row = row0 + (idx - j * rows_per);
             const uint32_t off = static_cast<uint32_t>((row * kRedStride + j) * 4);
+            float part[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q)  // all remote loads in flight, then a fixed-order sum
+                part[q] = q < splits ? ld_shared_cluster_f32(map_shared_rank(red_addr + off, q)) : 0.0f;
             float sum = 0.0f;
-            for (int q = 0; q < splits; ++q) sum += ld_shared_cluster_f32(map_shared_rank(red_addr + off, q));
+#pragma unroll
+            for (int q = 0; q < 8; ++q) sum += part[q];
             const int n = n0 + row;
             if (n < N) y[static_cast<int64_t>(j) * N + n] = __float2bfloat16_rn(sum);
         }
@@ -248,22 +267,25 @@ cudaError_t launch_variant(const void *qa, const float *sa, const void *qw, cons
 
     const int64_t nblocks = (N + kRows - 1) / kRows;
     const int64_t Kg = (K + BK - 1) / BK;
-    // Split K over a cluster until about two CTAs per SM are in flight.
+    // Split K over a cluster as far as all CTAs still fit on the GPU at once
+    // (two per SM), so that no CTA waits for a second wave.
     int splits = 1;
-    while (splits < 8 && nblocks * splits < 2 * dev.sm_count && splits * 2 <= Kg) splits *= 2;
+    while (splits < 8 && nblocks * splits * 2 <= 2 * dev.sm_count && splits * 2 <= Kg) splits *= 2;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(nblocks * splits));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = static_cast<unsigned>(splits);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, gemm_decode_kernel<PER_TENSOR>, tmW, tmX, sa, sw,
                               static_cast<__nv_bfloat16 *>(y), static_cast<int>(M), static_cast<int>(N),
                               static_cast<int>(K), splits, dev.err);

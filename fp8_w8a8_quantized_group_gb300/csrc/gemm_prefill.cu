@@ -46,8 +46,8 @@ constexpr int kTmemCols = 512;
 // Register split: warpgroup 0 shrinks, the two epilogue warpgroups grow.
 // 128 * kRegsLow + 256 * kRegsHigh must not exceed 384 * (registers the
 // kernel is compiled with); the launcher checks that before every launch.
-constexpr int kRegsLow = 80;
-constexpr int kRegsHigh = 200;
+constexpr int kRegsLow = 72;
+constexpr int kRegsHigh = 216;
 
 // Bounded-wait sites reported through the error word.
 enum : unsigned { kSiteProdEmpty = 101, kSiteMmaTmem = 102, kSiteMmaFull = 103, kSiteEpiFull = 104,
@@ -277,28 +277,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int nb = (tl.n0 + c0) / 128;  // this half lies in one 128-column weight block
                 const float *swp = sw + (static_cast<int64_t>(tl.group) * Nb + (nb < Nb ? nb : Nb - 1)) * Kg;
                 const float *sap = sa + m;
-                float sa_next = row_in ? __ldg(sap) : 0.0f;
-                float sw_next = __ldg(swp);
+                // Scales of K blocks kb+1 and kb+2 are in flight while block kb is promoted.
+                float sa1 = row_in ? __ldg(sap) : 0.0f, sw1 = __ldg(swp);
+                float sa2 = (row_in && Kg > 1) ? __ldg(sap + M) : 0.0f, sw2 = Kg > 1 ? __ldg(swp + 1) : 0.0f;
                 for (int kb = 0; kb < Kg; ++kb) {
-                    const float sc = sa_next * sw_next;
-                    if (kb + 1 < Kg) {  // next block's scales, in flight during this block
-                        sa_next = row_in ? __ldg(sap + static_cast<int64_t>(kb + 1) * M) : 0.0f;
-                        sw_next = __ldg(swp + kb + 1);
+                    const float sc = sa1 * sw1;
+                    sa1 = sa2;
+                    sw1 = sw2;
+                    if (kb + 2 < Kg) {
+                        sa2 = row_in ? __ldg(sap + static_cast<int64_t>(kb + 2) * M) : 0.0f;
+                        sw2 = __ldg(swp + kb + 2);
                     }
                     ok = __all_sync(0xffffffffu, mbar_wait(&tfull[buf], bphase, abort_flag, err, kSiteEpiFull));
                     if (!ok) break;
                     tc_fence_after();
+                    // 64-column loads (two in flight per wait): two waits per K
+                    // block for BN = 256, one for BN = 128.
+                    const uint32_t base = lane_addr + buf * BN;
 #pragma unroll
-                    for (int c = 0; c < C::kCols / C::kChunk; ++c) {
-                        float p[C::kChunk];
-                        tmem_ld_chunk<C::kChunk>(lane_addr + buf * BN + c * C::kChunk, p);
-                        if (c == C::kCols / C::kChunk - 1) {  // all of this buffer is in registers
+                    for (int c = 0; c < C::kCols / 64; ++c) {
+                        float p[64];
+                        tmem_ld64(base + c * 64, p);
+                        if (c == C::kCols / 64 - 1) {  // every chunk of this buffer is in registers
                             tc_fence_before();
                             mbar_arrive(&tempty[buf]);
                         }
 #pragma unroll
-                        for (int j = 0; j < C::kChunk; ++j)
-                            acc[c * C::kChunk + j] = fmaf(p[j], sc, acc[c * C::kChunk + j]);
+                        for (int j = 0; j < 64; ++j) acc[c * 64 + j] = fmaf(p[j], sc, acc[c * 64 + j]);
                     }
                     if (++buf == C::kBufs) { buf = 0; bphase ^= 1u; }
                 }

@@ -2,7 +2,9 @@
 //
 //  - 1 x 128 activation groups (dynamic, per token): one half-warp per group,
 //    16-byte loads of 8 BF16 per lane, shuffle amax over the half-warp,
-//    8-byte stores of 8 packed codes per lane.
+//    8-byte stores of 8 packed codes per lane; launched as a programmatic
+//    dependent so that, in a decode step, its launch overlaps the previous
+//    GEMM and the next GEMM's prologue overlaps it.
 //  - 128 x 128 weight blocks: one CTA per block, the block held in registers
 //    between the amax pass and the quantize pass (read once).
 //  - Per tensor: grid-wide amax (atomicMax on the bit pattern of the
@@ -34,6 +36,10 @@ __global__ void __launch_bounds__(kActThreads) quant_act_group_kernel(const uint
     const int hw = threadIdx.x >> 4;
     const int hl = threadIdx.x & 15;
     const int64_t base = static_cast<int64_t>(blockIdx.x) * kActGroupsPerBlock;
+    // Launched as a programmatic dependent: let the next kernel start its
+    // prologue, then wait for the kernel that produced x.
+    grid_dep_launch();
+    grid_dep_wait();
 
     uint4 v[kActUnroll];
     int64_t off[kActUnroll];
@@ -197,9 +203,17 @@ cudaError_t launch_quant_act_group(const void *x, void *q, float *s, int64_t M, 
     const int64_t blocks = (items + kActGroupsPerBlock - 1) / kActGroupsPerBlock;
     if (blocks == 0) return cudaSuccess;
     if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
-    quant_act_group_kernel<<<static_cast<unsigned>(blocks), kActThreads, 0, stream>>>(
-        static_cast<const uint16_t *>(x), static_cast<uint8_t *>(q), s, M, K);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(kActThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, quant_act_group_kernel, static_cast<const uint16_t *>(x),
+                              static_cast<uint8_t *>(q), s, M, K);
 }
 
 cudaError_t launch_quant_weight_block(const void *w, void *q, float *s, int64_t N, int64_t K,
