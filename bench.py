@@ -61,6 +61,20 @@ def tensor_gemm_bytes(M, N, K):
     return N * K + M * K + 2 * M * N + 8
 
 
+def whole_job(step_units: float, ms_per_step: float, world: int, dist=None, device="cpu"):
+    """Whole-job throughput over all ranks: units every rank processed per step,
+    summed, over the slowest rank's step time. Returns (units per second,
+    max ms per step). With world > 1 it all-reduces through `dist`."""
+    if world > 1:
+        import torch
+        t = torch.tensor([ms_per_step], dtype=torch.float64, device=device)
+        u = torch.tensor([step_units], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dist.all_reduce(u, op=dist.ReduceOp.SUM)
+        ms_per_step, step_units = t.item(), u.item()
+    return step_units / (ms_per_step * 1e-3), ms_per_step
+
+
 # ----------------------------------------------------------------- clocks --
 
 class ClockSampler:
@@ -285,7 +299,7 @@ def run_decode_section(torch, ops, dev, steps, warmup, peaks, sync_ranks):
             us = t * 1e3 / (reps * LAYERS)
             per_shape[f"M{M}_N{N}_K{K}"] = {"us": us, "GBps": gemm_bytes(M, N, K) / (us * 1e-6) / 1e9}
     out = {"value": value, "ms_per_step": ms / steps, "roofline": roof, "per_shape": per_shape,
-           "launches_per_step": 2 * len(calls), "window": window}
+           "launches_per_step": 2 * len(calls), "window": window, "step_bytes": step_bytes}
 
     # end to end: host activations (pinned) -> device -> quantize -> GEMM -> host output
     host_x = {k: v[0].cpu().pin_memory() for k, v in acts.items()}
@@ -590,8 +604,13 @@ def run_case(spec: str, launches: int):
         e1.record()
         torch.cuda.synchronize()
         times.append(e0.elapsed_time(e1) * 1e3)
+    # device time per launch: a graph of back-to-back launches, replayed
+    reps = 20
+    g = Timed(torch, lambda marks: [fn() for _ in range(reps)])
+    ms, _ = time_steps(torch, g.replay, 5, 2)
+    graph_us = ms * 1e3 / (5 * reps)
     code, site = ops.fp8_device_error()
-    print(json.dumps({"case": spec, "us": times, "device_error": code}))
+    print(json.dumps({"case": spec, "us": times, "graph_us": graph_us, "device_error": code}))
     if code:
         raise SystemExit(1)
 
@@ -653,14 +672,9 @@ def main():
         sampler.stop()
     clocks = sampler.summary(*dec["window"])
 
-    # whole-job value: max time over ranks, units of all ranks
-    ms_step = dec["ms_per_step"]
-    value = dec["value"]
-    if world > 1:
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = t.item()
-        value = dec["value"] * dec["ms_per_step"] / ms_step * world
+    # whole-job value: units of all ranks over the slowest rank's time
+    bytes_per_s, ms_step = whole_job(dec["step_bytes"], dec["ms_per_step"], world, dist, dev)
+    value = bytes_per_s / 1e9
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()

@@ -23,36 +23,32 @@ namespace {
 // ------------------------------------------------ 1 x 128 activation groups --
 
 constexpr int kActThreads = 256;
-constexpr int kActUnroll = 4;                       // groups per half-warp
-constexpr int kActGroupsPerBlock = (kActThreads / 16) * kActUnroll;
+constexpr int kActRows = kActThreads / 16;          // rows per CTA: one half-warp each
+constexpr int kActUnroll = 4;                       // consecutive groups per half-warp
 
-// Item i = g * M + m (m fastest): row m, K-group g. Half-warp h of the block
-// takes items base + u * 16 + h for u < kActUnroll.
+// CTA (blockIdx.x, blockIdx.y) covers rows 16*blockIdx.x .. +15 and groups
+// 4*blockIdx.y .. +3; half-warp h takes row 16*blockIdx.x + h and reads its
+// four groups (1 KB of the row) with four 16-byte loads per lane in flight.
 __global__ void __launch_bounds__(kActThreads) quant_act_group_kernel(const uint16_t *__restrict__ x,
                                                                       uint8_t *__restrict__ q,
                                                                       float *__restrict__ s, int64_t M,
                                                                       int64_t K) {
-    const int64_t items = M * (K / 128);
+    const int64_t Kg = K / 128;
     const int hw = threadIdx.x >> 4;
     const int hl = threadIdx.x & 15;
-    const int64_t base = static_cast<int64_t>(blockIdx.x) * kActGroupsPerBlock;
+    const int64_t m = static_cast<int64_t>(blockIdx.x) * kActRows + hw;
+    const int64_t g0 = static_cast<int64_t>(blockIdx.y) * kActUnroll;
     // Launched as a programmatic dependent: let the next kernel start its
     // prologue, then wait for the kernel that produced x.
     grid_dep_launch();
     grid_dep_wait();
 
     uint4 v[kActUnroll];
-    int64_t off[kActUnroll];
+    const bool row_ok = m < M;
 #pragma unroll
     for (int u = 0; u < kActUnroll; ++u) {
-        const int64_t it = base + u * 16 + hw;
         v[u] = make_uint4(0u, 0u, 0u, 0u);
-        off[u] = -1;
-        if (it < items) {
-            const int64_t g = it / M, m = it - g * M;
-            off[u] = m * K + g * 128 + hl * 8;
-            v[u] = ld_stream_v4(x + off[u]);
-        }
+        if (row_ok && g0 + u < Kg) v[u] = ld_stream_v4(x + m * K + (g0 + u) * 128 + hl * 8);
     }
 #pragma unroll
     for (int u = 0; u < kActUnroll; ++u) {
@@ -61,10 +57,10 @@ __global__ void __launch_bounds__(kActThreads) quant_act_group_kernel(const uint
         a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
         a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
         a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-        if (off[u] >= 0) {
+        if (row_ok && g0 + u < Kg) {
             const float sc = block_scale(a);
-            *reinterpret_cast<uint2 *>(q + off[u]) = quant8(v[u], sc);
-            if (hl == 0) s[base + u * 16 + hw] = sc;  // s[g * M + m] == s[item]
+            *reinterpret_cast<uint2 *>(q + m * K + (g0 + u) * 128 + hl * 8) = quant8(v[u], sc);
+            if (hl == 0) s[(g0 + u) * M + m] = sc;
         }
     }
 }
@@ -199,12 +195,12 @@ __global__ void __launch_bounds__(1024) tensor_quant_small_kernel(const uint16_t
 cudaError_t launch_quant_act_group(const void *x, void *q, float *s, int64_t M, int64_t K,
                                    const DeviceInfo &dev, cudaStream_t stream) {
     (void)dev;
-    const int64_t items = M * (K / 128);
-    const int64_t blocks = (items + kActGroupsPerBlock - 1) / kActGroupsPerBlock;
-    if (blocks == 0) return cudaSuccess;
-    if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    const int64_t rows = (M + kActRows - 1) / kActRows;
+    const int64_t cols = (K / 128 + kActUnroll - 1) / kActUnroll;
+    if (rows == 0 || cols == 0) return cudaSuccess;
+    if (rows > 0x7FFFFFFF || cols > 65535) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.gridDim = dim3(static_cast<unsigned>(rows), static_cast<unsigned>(cols));
     cfg.blockDim = dim3(kActThreads);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

@@ -105,3 +105,34 @@ def test_every_bf16_pattern_through_static_quantization(scale):
     nan = np.isnan(xf)
     assert np.array_equal(qg[~nan], qo[~nan])
     assert np.all((qg[nan] & 0x7F) == 0x7F)
+
+
+def _boundary_scales():
+    """Scales that put x/s within a few FP32 ulps of E4M3 rounding midpoints for
+    many BF16 x (x = a BF16 value, m = an E4M3 midpoint, s = x/m nudged by
+    k ulps), plus seeded random scales over many binades."""
+    import torch as _t
+    vals = _t.arange(256, dtype=_t.int32).to(_t.uint8).view(_t.float8_e4m3fn).to(_t.float64).numpy()[:0x7F]
+    mids = (vals[:-1] + vals[1:]) / 2
+    rng = np.random.default_rng(11)
+    out = []
+    for _ in range(12):
+        x = float(synth.bf16_bits_to_f32(synth.to_bf16(rng.uniform(0.1, 100.0, 1)))[0])
+        m = float(rng.choice(mids[8:]))
+        s = np.float32(x / m)
+        for k in (-3, -1, 0, 1, 3):
+            out.append(float(np.float32(s) + np.float32(k) * np.spacing(np.float32(s))))
+    out += [float(v) for v in np.exp2(rng.uniform(-40, 40, 12)).astype(np.float32)]
+    return out
+
+
+@pytest.mark.parametrize("scale", _boundary_scales())
+def test_rounding_boundaries_bit_exact(scale):
+    """Codes equal the oracle's (correctly rounded division, then E4M3) also when
+    x/s falls next to a rounding midpoint."""
+    x = np.arange(65536, dtype=np.uint32).astype(np.uint16).reshape(4096, 16)
+    keep = ~np.isnan(synth.bf16_bits_to_f32(x))
+    sc = np.float32(scale)
+    q, _ = ops.quant_per_tensor(to_dev_bf16(x), scale=torch.tensor([sc], device="cuda"))
+    qo, _ = oracle.quant_per_tensor(x, scale=sc)
+    assert np.array_equal(q.cpu().numpy()[keep], qo[keep])
