@@ -148,21 +148,28 @@ def _peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
-def _traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current source of the kernel (else None)."""
+def _traffic(kernel: str, algorithmic_bytes_per_launch: float):
+    """DRAM bytes (read + write) per launch of `kernel`, from the committed ncu
+    captures in profiles/traffic.json: the captured DRAM/algorithmic ratio
+    (averaged over the captured shapes) times this launch's algorithmic bytes.
+    None if the kernel's sources changed since the capture (sha256 check)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
-        entries = json.load(f)
-    e = entries.get(f"{kernel}|{workload}")
+        e = json.load(f).get(kernel)
     if not e:
         return None
-    src = os.path.join(ROOT, e["source"])
-    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest() != e["sha256"]:
+    d = hashlib.sha256()
+    for src in e["sources"]:
+        full = os.path.join(ROOT, src)
+        if not os.path.exists(full):
+            return None
+        d.update(open(full, "rb").read())
+    if d.hexdigest() != e["sha256"]:
         return None
-    return e["bytes_per_launch"]
+    ratios = [c["ratio"] for c in e["captures"].values()]
+    return sum(ratios) / len(ratios) * algorithmic_bytes_per_launch
 
 
 # ------------------------------------------------------------ graph utils --
@@ -289,7 +296,8 @@ def run_decode_section(torch, ops, dev, steps, warmup, peaks, sync_ranks):
             "avg_launch_us": launch_ms * 1e3,
             "timing": "events around replays of a graph of the step's 96 GEMM launches"}
     roof["frac"] = roof["achieved"] / peaks["hbm_gbs"]
-    roof["traffic"] = _traffic("gemm_decode_kernel", "decode M16 N28672 K4096")
+    roof["traffic"] = _traffic("gemm_decode_kernel", gemm_total_bytes / len(calls))
+    roof["traffic_note"] = "ncu dram read+write per launch, captured ratio x this mix's algorithmic bytes"
     per_shape = {}
     for M in DECODE_M:
         for i, (N, K) in enumerate(SHAPES):
@@ -372,7 +380,8 @@ def run_prefill_section(torch, ops, dev, steps, warmup, peaks):
            "roofline": {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
                         "frac": achieved / fp8_peak if achieved else None,
                         "peak_source": f"bf16_tflops of {peaks['source']} x {FP8_OVER_BF16} (nominal FP8/BF16)",
-                        "traffic": _traffic("gemm_prefill_kernel", "prefill M8192 N4096 K4096")},
+                        "traffic": _traffic("gemm_prefill_kernel", sum(
+                            M * K + N * K + 2 * M * N + 4 * M * K // 128 for (M, N, K, *_r) in calls) / len(calls))},
            "per_shape": per, "ms_per_step_incl_l2_flush": ms / steps,
            "l2": "256 MB buffer written between GEMMs, outside the kernel events"}
     del calls, weights, flush
