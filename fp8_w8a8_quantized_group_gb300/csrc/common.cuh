@@ -387,6 +387,14 @@ __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
     return v;
 }
 
+__device__ __forceinline__ float4 ld_shared_cluster_f32x4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
 // ------------------------------------------------------------------- BF16 --
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

@@ -42,9 +42,10 @@ constexpr int kWBytes = kRows * BK;
 constexpr int kXBytes = kTok * BK;
 constexpr int kThreads = 256;
 constexpr int kTmemCols = 32;   // two 16-column partial buffers
-constexpr int kRedStride = kTok + 1;
 constexpr int kL2Warm = 8;      // weight tiles warmed in L2 before the upstream grid completes
-constexpr int kSmemBytes = 1024 + kStages * (kWBytes + kXBytes) + 8 * (2 * kStages + 4) + 16;
+constexpr int kScaleKb = 8;     // K blocks of activation/weight scales staged at a time per epilogue warp
+constexpr int kScaleBytes = 4 * 4 * (kScaleKb * kTok + kScaleKb);
+constexpr int kSmemBytes = 1024 + kStages * (kWBytes + kXBytes) + 8 * (2 * kStages + 4) + 16 + kScaleBytes;
 
 enum : unsigned { kSiteProdEmpty = 201, kSiteMmaTmem = 202, kSiteMmaFull = 203, kSiteEpiFull = 204,
                   kSiteDrain = 205 };
@@ -65,6 +66,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     float *red = reinterpret_cast<float *>(sW);  // reused after the main loop
+    float *scale_smem = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(tmem_slot) + 16);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nb = blockIdx.x / splits;
@@ -166,21 +168,49 @@ __global__ void __launch_bounds__(kThreads, 2)
         uint32_t buf = 0, bphase = 0;
         grid_dep_wait();
         if (!PER_TENSOR) {
+            // Scales of kScaleKb K blocks at a time go through this warp's own
+            // shared-memory slice; the next chunk is loaded into registers while
+            // the current one is used (one L2 round trip per chunk, not per block).
             const float *swrow = sw + static_cast<int64_t>(nb) * Kg;
-            for (int kb = kb0; kb < kb1; ++kb) {
-                const float wscale = __ldg(swrow + kb);
-                float sav[kTok];
+            float *w_sa = scale_smem + ep * (kScaleKb * kTok + kScaleKb);
+            float *w_sw = w_sa + kScaleKb * kTok;
+            float r_sa[kScaleKb * kTok / 32], r_sw = 0.0f;
+            auto fetch = [&](int c0) {
+                const int n = (min(kb1, c0 + kScaleKb) - c0);
 #pragma unroll
-                for (int j = 0; j < kTok; ++j) sav[j] = j < M ? __ldg(sa + static_cast<int64_t>(kb) * M + j) : 0.0f;
-                if (!__all_sync(0xffffffffu, mbar_wait(&tfull[buf], bphase, abort_flag, err, kSiteEpiFull))) break;
-                tc_fence_after();
-                float p[kTok];
-                tmem_ld16(lane_addr + buf * kTok, p);
-                tc_fence_before();
-                mbar_arrive(&tempty[buf]);
-                if (++buf == 2) { buf = 0; bphase ^= 1u; }
+                for (int i = 0; i < kScaleKb * kTok / 32; ++i) {
+                    const int idx = lane + 32 * i;
+                    r_sa[i] = idx < n * M ? __ldg(sa + static_cast<int64_t>(c0) * M + idx) : 0.0f;
+                }
+                r_sw = lane < n ? __ldg(swrow + c0 + lane) : 0.0f;
+            };
+            fetch(kb0);
+            bool ok = true;
+            for (int c0 = kb0; c0 < kb1 && ok; c0 += kScaleKb) {
+                __syncwarp();
 #pragma unroll
-                for (int j = 0; j < kTok; ++j) acc[j] = fmaf(p[j], wscale * sav[j], acc[j]);
+                for (int i = 0; i < kScaleKb * kTok / 32; ++i) w_sa[lane + 32 * i] = r_sa[i];
+                if (lane < kScaleKb) w_sw[lane] = r_sw;
+                __syncwarp();
+                if (c0 + kScaleKb < kb1) fetch(c0 + kScaleKb);
+                const int c1 = min(kb1, c0 + kScaleKb);
+                for (int kb = c0; kb < c1; ++kb) {
+                    const float wscale = w_sw[kb - c0];
+                    const float *srow = w_sa + (kb - c0) * M;
+                    if (!__all_sync(0xffffffffu, mbar_wait(&tfull[buf], bphase, abort_flag, err, kSiteEpiFull))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    float p[kTok];
+                    tmem_ld16(lane_addr + buf * kTok, p);
+                    tc_fence_before();
+                    mbar_arrive(&tempty[buf]);
+                    if (++buf == 2) { buf = 0; bphase ^= 1u; }
+#pragma unroll
+                    for (int j = 0; j < kTok; ++j)
+                        if (j < M) acc[j] = fmaf(p[j], wscale * srow[j], acc[j]);
+                }
             }
         } else {
             if (__all_sync(0xffffffffu, mbar_wait(&tfull[0], 0, abort_flag, err, kSiteEpiFull))) {
@@ -214,27 +244,43 @@ __global__ void __launch_bounds__(kThreads, 2)
         __syncthreads();
         if (warp >= 4) {
             const int r = (warp - 4) * 32 + lane;
+            float4 *dst = reinterpret_cast<float4 *>(red + r * kTok);
 #pragma unroll
-            for (int j = 0; j < kTok; ++j) red[r * kRedStride + j] = acc[j];
+            for (int j = 0; j < kTok / 4; ++j)
+                dst[j] = make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
         }
         cluster_sync_all();
+        // CTA `rank` sums rows [rank*rows_per, +rows_per) over the cluster: one
+        // thread per (row, 4 tokens), 16-byte remote loads from every rank, all
+        // in flight, then a fixed-order sum.
         const uint32_t rank = cluster_ctarank();
         const int rows_per = kRows / splits;
         const int row0 = static_cast<int>(rank) * rows_per;
+        const int quads = (M + 3) / 4;
         const uint32_t red_addr = smem_u32(red);
-        for (int idx = threadIdx.x; idx < rows_per * M; idx += kThreads) {
-            const int j = idx / rows_per;
-            const int row = row0 + (idx - j * rows_per);
-            const uint32_t off = static_cast<uint32_t>((row * kRedStride + j) * 4);
-            float part[8];
+        for (int idx = threadIdx.x; idx < rows_per * quads; idx += kThreads) {
+            const int qd = idx / rows_per;
+            const int row = row0 + (idx - qd * rows_per);
+            const uint32_t off = static_cast<uint32_t>((row * kTok + qd * 4) * 4);
+            float4 part[8];
 #pragma unroll
-            for (int q = 0; q < 8; ++q)  // all remote loads in flight, then a fixed-order sum
-                part[q] = q < splits ? ld_shared_cluster_f32(map_shared_rank(red_addr + off, q)) : 0.0f;
-            float sum = 0.0f;
+            for (int q = 0; q < 8; ++q)
+                part[q] = q < splits ? ld_shared_cluster_f32x4(map_shared_rank(red_addr + off, q))
+                                     : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            float sum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-            for (int q = 0; q < 8; ++q) sum += part[q];
+            for (int q = 0; q < 8; ++q) {
+                sum[0] += part[q].x;
+                sum[1] += part[q].y;
+                sum[2] += part[q].z;
+                sum[3] += part[q].w;
+            }
             const int n = n0 + row;
-            if (n < N) y[static_cast<int64_t>(j) * N + n] = __float2bfloat16_rn(sum);
+            if (n < N) {
+#pragma unroll
+                for (int t = 0; t < 4; ++t)
+                    if (qd * 4 + t < M) y[static_cast<int64_t>(qd * 4 + t) * N + n] = __float2bfloat16_rn(sum[t]);
+            }
         }
         cluster_sync_all();
     }
