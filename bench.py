@@ -6,8 +6,11 @@ block-scaled layer: M in {1, 4, 16} tokens through the four Llama-8B-like
 projections (N, K) in {(4096,4096), (6144,4096), (28672,4096), (4096,14336)},
 over a stack of layers with distinct weights so that every pass streams far
 more weight bytes than the 129 MB L2 holds. One step = for every M, layer and
-projection: dynamic 1x128 activation quantization + block-scaled GEMM. The
-metric is HBM GB/s of algorithmic bytes (codes, scales, activations, output).
+projection: dynamic 1x128 activation quantization + block-scaled GEMM, through
+fp8_block_linear (a quantization launch and a GEMM launch per call, chained
+by programmatic dependent launch). The metric is HBM GB/s of algorithmic
+bytes (weights and scales, BF16 activations in, codes and scales out, BF16
+output).
 
 The same run also times, as extra sections, the prefill-shaped GEMMs
 (TFLOPS vs the FP8 tensor peak), the per-tensor layer, the MoE grouped GEMM
@@ -55,6 +58,13 @@ def gemm_bytes(M, N, K):
 def act_quant_bytes(M, K):
     """BF16 read + E4M3 write + one FP32 scale per 128 values."""
     return 2 * M * K + M * K + 4 * M * (K // 128)
+
+
+def linear_bytes(M, N, K):
+    """Algorithmic bytes of one W8A8 linear call from BF16 activations: Qw + Sw,
+    X (BF16) in, activation codes + scales out, Y (BF16) out."""
+    nb, kg = -(-N // 128), K // 128
+    return N * K + 4 * nb * kg + 2 * M * K + M * K + 4 * M * kg + 2 * M * N
 
 
 def tensor_gemm_bytes(M, N, K):
@@ -267,12 +277,11 @@ def run_decode_section(torch, ops, dev, steps, warmup, peaks, sync_ranks):
             N, K = SHAPES[i]
             x, qa, sa, ys = acts[(M, N, K)]
             qw, sw = layers[layer][i]
-            ops.fp8_quant_act_group(x, qa, sa)
-            ops.fp8_block_gemm(qa, sa, qw, sw, ys[layer])
+            ops.fp8_block_linear(x, qa, sa, qw, sw, ys[layer])
 
     timed = Timed(torch, step)
     ms, window = time_steps(torch, timed.replay, steps, warmup, sync_ranks)
-    step_bytes = sum(gemm_bytes(M, *SHAPES[i]) + act_quant_bytes(M, SHAPES[i][1]) for M, _, i in calls)
+    step_bytes = sum(linear_bytes(M, *SHAPES[i]) for M, _, i in calls)
     gemm_total_bytes = sum(gemm_bytes(M, *SHAPES[i]) for M, _, i in calls)
     value = step_bytes * steps / (ms * 1e-3) / 1e9
 
@@ -321,8 +330,7 @@ def run_decode_section(torch, ops, dev, steps, warmup, peaks, sync_ranks):
             x, qa, sa, ys = acts[(M, N, K)]
             x.copy_(host_x[(M, N, K)], non_blocking=True)
             qw, sw = layers[layer][i]
-            ops.fp8_quant_act_group(x, qa, sa)
-            ops.fp8_block_gemm(qa, sa, qw, sw, ys[layer])
+            ops.fp8_block_linear(x, qa, sa, qw, sw, ys[layer])
             host_y[(M, N, K)][layer].copy_(ys[layer], non_blocking=True)
 
     e2e_steps = max(1, min(steps, 20))
@@ -522,7 +530,7 @@ def oracle_decode_sample(budget_s: float):
         qa, sa = oracle.quant_act_group(x)
         oracle.gemm_block_points(qa, sa, qw, sw, np.zeros(n, np.int64), np.arange(n))
         t_total += time.perf_counter() - t0
-        nbytes += gemm_bytes(1, n, K) + act_quant_bytes(1, K)
+        nbytes += linear_bytes(1, n, K)
         cols_used.append(n)
     desc = (f"M=1 decode: activation quantization + FP64 GEMM on the first {cols_used} output columns of the "
             f"four projections (one layer), single-threaded C oracle")
@@ -556,7 +564,7 @@ def reference_arm(args):
 
 def run_case(spec: str, launches: int):
     """One kernel on one shape, for profiling: KIND:M:N:K with KIND in
-    decode|prefill|tensor|moe|act|weight|ptensor. Prints per-launch times."""
+    decode|prefill|linear|tensor|moe|act|weight|ptensor. Prints per-launch times."""
     import torch
 
     import __graft_entry__
@@ -572,6 +580,12 @@ def run_case(spec: str, launches: int):
         qw, sw = ops.quant_weight_block(synth.device_normal_bf16(N, K, 0, "case/W", sigma=0.02, device=dev))
         y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
         fn = lambda: ops.fp8_block_gemm(qa, sa, qw, sw, y)  # noqa: E731
+    elif kind == "linear":
+        qa = torch.empty((M, K), dtype=torch.uint8, device=dev)
+        sa = torch.empty((K // 128, M), dtype=torch.float32, device=dev)
+        qw, sw = ops.quant_weight_block(synth.device_normal_bf16(N, K, 0, "case/W", sigma=0.02, device=dev))
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        fn = lambda: ops.fp8_block_linear(x, qa, sa, qw, sw, y)  # noqa: E731
     elif kind == "tensor":
         qa, sa = ops.quant_per_tensor(x)
         qw, sw = ops.quant_per_tensor(synth.device_normal_bf16(N, K, 0, "case/W", sigma=0.02, device=dev))

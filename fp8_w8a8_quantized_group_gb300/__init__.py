@@ -8,7 +8,9 @@ the first call does, and raises if the library is missing.
 from .ops import (  # noqa: F401
     Fp8Error,
     block_gemm,
+    block_linear,
     fp8_block_gemm,
+    fp8_block_linear,
     fp8_device_error,
     fp8_quant_act_group,
     fp8_quant_per_tensor,

@@ -26,6 +26,7 @@ SIGNATURES = {
     "fp8_quant_per_tensor": ([P, P, P, I64, I64, I32, P], I32),
     "fp8_block_gemm": ([P, P, P, P, P, I64, I64, I64, I32, I32, I32, I32, P, P], I32),
     "fp8_tensor_gemm": ([P, P, P, P, P, I64, I64, I64, P], I32),
+    "fp8_block_linear": ([P, P, P, P, P, P, I64, I64, I64, P], I32),
     "fp8_status_string": ([I32], ctypes.c_char_p),
     "fp8_device_error": ([P, ctypes.POINTER(I32), ctypes.POINTER(I32)], I32),
 }

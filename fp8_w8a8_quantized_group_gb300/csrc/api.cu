@@ -174,6 +174,25 @@ int fp8_tensor_gemm(const void *qa, const float *sa, const void *qw, const float
         fp8k::launch_gemm_prefill(qa, sa, qw, sw, y_bf16, M, N, K, 1, nullptr, true, *dev, s));
 }
 
+int fp8_block_linear(const void *x_bf16, void *qa, float *sa, const void *qw, const float *sw, void *y_bf16,
+                     int64_t M, int64_t N, int64_t K, void *stream) {
+    if (M < 0 || N < 0 || K < 0) return FP8_ERR_SHAPE;
+    if (K == 0 || K % FP8_GROUP != 0 || N == 0 || N % 16 != 0) return FP8_ERR_SHAPE;
+    if (M > INT_MAX || N > INT_MAX || K > INT_MAX) return FP8_ERR_SHAPE;
+    if (M == 0) return FP8_OK;
+    if (!x_bf16 || !qa || !sa || !qw || !sw || !y_bf16) return FP8_ERR_NULL;
+    if (misaligned(x_bf16, 16) || misaligned(qa, 16) || misaligned(qw, 16) || misaligned(y_bf16, 16) ||
+        misaligned(sa, 4) || misaligned(sw, 4))
+        return FP8_ERR_ALIGN;
+    const fp8k::DeviceInfo *dev = nullptr;
+    if (int st = fp8k::current_device(&dev)) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = fp8k::launch_quant_act_group(x_bf16, qa, sa, M, K, *dev, s);
+    if (e != cudaSuccess) return FP8_ERR_CUDA;
+    if (M <= 16) return fp8k::to_status(fp8k::launch_gemm_decode(qa, sa, qw, sw, y_bf16, M, N, K, false, *dev, s));
+    return fp8k::to_status(fp8k::launch_gemm_prefill(qa, sa, qw, sw, y_bf16, M, N, K, 1, nullptr, false, *dev, s));
+}
+
 const char *fp8_status_string(int status) {
     switch (status) {
         case FP8_OK: return "ok";

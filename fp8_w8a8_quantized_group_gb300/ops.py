@@ -96,6 +96,15 @@ def fp8_tensor_gemm(qa, sa, qw, sw, y, stream=None) -> None:
            "fp8_tensor_gemm")
 
 
+def fp8_block_linear(x, qa, sa, qw, sw, y, stream=None) -> None:
+    M, K = x.shape
+    N = y.shape[1]
+    _check(_lib.load().fp8_block_linear(_ptr(x, torch.bfloat16, "x"), _ptr(qa, torch.uint8, "qa"),
+                                        _ptr(sa, torch.float32, "sa"), _ptr(qw, torch.uint8, "qw"),
+                                        _ptr(sw, torch.float32, "sw"), _ptr(y, torch.bfloat16, "y"), M, N, K,
+                                        _stream(stream)), "fp8_block_linear")
+
+
 def fp8_status_string(status: int) -> str:
     return _lib.load().fp8_status_string(status).decode()
 
@@ -148,6 +157,17 @@ def block_gemm(qa, sa, qw, sw, group_offsets=None, stream=None) -> torch.Tensor:
     groups = qw.shape[0] if qw.dim() == 3 else 1
     fp8_block_gemm(qa, sa, qw, sw, y, num_groups=groups, group_offsets=group_offsets, stream=stream)
     return y
+
+
+def block_linear(x, qw, sw, stream=None):
+    """BF16 [M, K] x quantized weights -> (Y BF16 [M, N], activation codes, scales)."""
+    M, K = x.shape
+    N = qw.shape[0]
+    qa = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    sa = torch.empty((K // GROUP, M), dtype=torch.float32, device=x.device)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    fp8_block_linear(x, qa, sa, qw, sw, y, stream=stream)
+    return y, qa, sa
 
 
 def tensor_gemm(qa, sa, qw, sw, stream=None) -> torch.Tensor:

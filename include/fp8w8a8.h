@@ -154,6 +154,27 @@ int fp8_block_gemm(const void *qa, const float *sa, const void *qw, const float 
 int fp8_tensor_gemm(const void *qa, const float *sa, const void *qw, const float *sw,
                     void *y_bf16, int64_t M, int64_t N, int64_t K, void *stream);
 
+/*
+ * W8A8 linear layer, Y = X * W^T, from BF16 activations: dynamic 1x128
+ * activation quantization (as fp8_quant_act_group) followed by the
+ * block-scaled GEMM (as fp8_block_gemm), dense.
+ *
+ *   x_bf16  [M][K] BF16, input.
+ *   qa      [M][K] E4M3 and sa [K/128][M] FP32: outputs, the activation codes
+ *           and scales (caller-owned; bit-identical to fp8_quant_act_group).
+ *   qw, sw  as fp8_block_gemm (block_n = block_k = group_k = 128).
+ *   y       [M][N] BF16, output.
+ *   K a positive multiple of 128, N a positive multiple of 16, M >= 0.
+ * Two launches on `stream`: the quantization kernel, then the decode
+ * (M <= 16) or prefill GEMM. The quantization kernel is a programmatic
+ * dependent of the work before it, and the GEMM of the quantization kernel:
+ * each starts its prologue (and the decode GEMM warms L2 with its weights)
+ * while its predecessor finishes, and waits for it before reading its output.
+ * Errors: NULL, SHAPE, ALIGN, DEVICE, CUDA.
+ */
+int fp8_block_linear(const void *x_bf16, void *qa, float *sa, const void *qw, const float *sw,
+                     void *y_bf16, int64_t M, int64_t N, int64_t K, void *stream);
+
 /* Static, NUL-terminated description of a status code. Never NULL. */
 const char *fp8_status_string(int status);
 

@@ -17,10 +17,10 @@ def lib():
     return _lib.load()
 
 
-def test_header_declares_five_entry_points():
+def test_header_declares_the_entry_points():
     names = _lib.header_functions()
     for n in ["fp8_quant_act_group", "fp8_quant_weight_block", "fp8_quant_per_tensor", "fp8_block_gemm",
-              "fp8_tensor_gemm"]:
+              "fp8_tensor_gemm", "fp8_block_linear"]:
         assert n in names
     assert set(names) == set(_lib.SIGNATURES)
 
@@ -95,6 +95,16 @@ def test_tensor_gemm_validation(lib):
     assert f(FAKE, FAKE, None, FAKE, FAKE, 4, 256, 256, None) == 1
     assert f(ODD, FAKE, FAKE, FAKE, FAKE, 4, 256, 256, None) == 3
     assert f(None, None, None, None, None, 0, 256, 256, None) == 0
+
+
+def test_block_linear_validation(lib):
+    f = lib.fp8_block_linear
+    ok6 = (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE)
+    assert f(*ok6, 4, 256, 200, None) == 2            # K % 128
+    assert f(*ok6, 4, 250, 256, None) == 2            # N % 16
+    assert f(FAKE, None, FAKE, FAKE, FAKE, FAKE, 4, 256, 256, None) == 1
+    assert f(FAKE, FAKE, FAKE + 2, FAKE, FAKE, FAKE, 4, 256, 256, None) == 3
+    assert f(None, None, None, None, None, None, 0, 256, 256, None) == 0
 
 
 def test_valid_call_without_gpu_fails_loudly(lib):

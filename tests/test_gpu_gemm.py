@@ -247,3 +247,41 @@ def test_tensor_gemm_matches_block_gemm_with_uniform_scales():
     yo, ab = oracle.gemm_tensor(qao, np.float32(0.013), qwo, np.float32(0.0007))
     assert_within_tolerance(yt, yo, ab, "tensor")
     assert_within_tolerance(yb, yo, ab, "block with uniform scales")
+
+
+# ---------------------------------------------------------- fused linear --
+
+@pytest.mark.parametrize("M,N,K", [(1, 256, 256), (3, 384, 1024), (16, 256, 256), (16, 4096, 4096),
+                                   (7, 272, 14336), (1, 28672, 4096), (40, 512, 512)])
+def test_block_linear_matches_separate_calls_and_oracle(M, N, K):
+    """fp8_block_linear writes the same activation codes and scales as
+    fp8_quant_act_group and the same Y, bit for bit, as fp8_block_gemm on them;
+    Y is within tolerance of the oracle."""
+    x, w = synth.block_case(M, N, K, seed=3)
+    xd = to_dev_bf16(x)
+    qw, sw = ops.quant_weight_block(to_dev_bf16(w))
+    y, qa, sa = ops.block_linear(xd, qw, sw)
+    qa2, sa2 = ops.quant_act_group(xd)
+    y2 = ops.block_gemm(qa2, sa2, qw, sw)
+    torch.cuda.synchronize()
+    assert torch.equal(qa, qa2) and torch.equal(sa.view(torch.int32), sa2.view(torch.int32))
+    assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
+    qao, sao = oracle.quant_act_group(x)
+    qwo, swo = oracle.quant_weight_block(w)
+    assert np.array_equal(qa.cpu().numpy(), qao) and np.array_equal(f32_bits(sa.cpu().numpy()), f32_bits(sao))
+    yg = bf16_to_f64(y)
+    if M * N * K <= 64 * 2 ** 20:
+        yo, ab = oracle.gemm_block(qao, sao, qwo, swo)
+        assert_within_tolerance(yg, yo, ab, f"linear {M}x{N}x{K}")
+    else:
+        ms, ns = _sample_points(M, N, n_random=2000)
+        yo, ab = oracle.gemm_block_points(qao, sao, qwo, swo, ms, ns)
+        assert_within_tolerance(yg[ms, ns], yo, ab, f"linear {M}x{N}x{K} sampled")
+
+
+def test_block_linear_repeated_calls_stable():
+    x, w = synth.block_case(16, 1024, 2048, seed=8)
+    xd = to_dev_bf16(x)
+    qw, sw = ops.quant_weight_block(to_dev_bf16(w))
+    outs = [ops.block_linear(xd, qw, sw)[0] for _ in range(3)]
+    assert all(torch.equal(o.view(torch.int16), outs[0].view(torch.int16)) for o in outs[1:])
