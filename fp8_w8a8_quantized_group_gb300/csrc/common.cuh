@@ -119,16 +119,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking probe of the phase (the thread is never suspended).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait until the phase with the given parity has completed. Gives up after
 // kWaitLimitNs, or as soon as *abort is set by another thread of the CTA;
 // on giving up it records FP8_ERR_TIMEOUT with `site`, sets *abort and
 // returns false.
+// SPIN: poll with test_wait (lowest wake-up latency, for single-lane roles on
+// the critical path) instead of the suspending try_wait.
+template <bool SPIN = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
                                           unsigned *err, unsigned site) {
-    if (mbar_try_wait(bar, parity)) return true;
+    auto poll = [&] { return SPIN ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity); };
+    if (poll()) return true;
     const uint64_t t0 = global_ns();
     for (uint32_t spin = 1;; ++spin) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (poll()) return true;
         if ((spin & 63u) == 0u) {
             if (*abort) return false;
             if (global_ns() - t0 > kWaitLimitNs) {

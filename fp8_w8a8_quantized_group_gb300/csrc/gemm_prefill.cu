@@ -208,6 +208,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         } else if (warp == 1 && lane == 0) {
             // ------------------------------------------------- MMA issuer --
+            // This lane is the critical path between the epilogue's release of
+            // a TMEM buffer and the next MMAs: it spins (test_wait) rather than
+            // sleeping in try_wait, which shortens every hand-off.
             constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
             uint32_t stage = 0, phase = 0, buf = 0, bphase = 0;
             uint32_t last_stage = 0, last_phase = 0;
@@ -215,11 +218,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 for (int kb = 0; kb < Kg && ok; ++kb) {
                     if (!PER_TENSOR || kb == 0) {
-                        ok = mbar_wait(&tempty[buf], bphase ^ 1u, abort_flag, err, kSiteMmaTmem);
+                        ok = mbar_wait<true>(&tempty[buf], bphase ^ 1u, abort_flag, err, kSiteMmaTmem);
                         if (!ok) break;
                         tc_fence_after();
                     }
-                    ok = mbar_wait(&full[stage], phase, abort_flag, err, kSiteMmaFull);
+                    ok = mbar_wait<true>(&full[stage], phase, abort_flag, err, kSiteMmaFull);
                     if (!ok) break;
                     tc_fence_after();
                     const uint32_t a0 = smem_u32(sA + stage * C::kABytes);
