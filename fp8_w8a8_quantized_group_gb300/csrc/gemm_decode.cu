@@ -124,16 +124,17 @@ __global__ void __launch_bounds__(kThreads, 2)
         grid_dep_wait();
         if (lane == 0) {
             // ------------------------------------------------------- MMA --
+            // spins (test_wait): the lane sits on the critical path of each K block
             constexpr uint32_t idesc = idesc_e4m3_f32(kRows, kTok);
             uint32_t stage = 0, phase = 0, buf = 0, bphase = 0, last_stage = 0, last_phase = 0;
             bool any = false;
             for (int kb = kb0; kb < kb1; ++kb) {
                 const bool first = kb == kb0, last = kb == kb1 - 1;
                 if (!PER_TENSOR || first) {
-                    if (!mbar_wait(&tempty[buf], bphase ^ 1u, abort_flag, err, kSiteMmaTmem)) break;
+                    if (!mbar_wait<true>(&tempty[buf], bphase ^ 1u, abort_flag, err, kSiteMmaTmem)) break;
                     tc_fence_after();
                 }
-                if (!mbar_wait(&full[stage], phase, abort_flag, err, kSiteMmaFull)) break;
+                if (!mbar_wait<true>(&full[stage], phase, abort_flag, err, kSiteMmaFull)) break;
                 tc_fence_after();
                 const uint32_t w0 = smem_u32(sW + stage * kWBytes);
                 const uint32_t x0 = smem_u32(sX + stage * kXBytes);
