@@ -13,7 +13,8 @@
 //  - warp 0 (one lane): TMA producer, fills a ring of shared-memory stages;
 //    one stage = one 128-wide K block of A (128 x 128 B) and B (BN x 128 B),
 //    both K-major with 128-byte swizzle;
-//  - warp 1: owns TMEM; one lane issues 4 tcgen05.mma (K = 32 each) per stage
+//  - warp 1 owns TMEM; one lane of warp 1 (and, block-scaled, one of warp 2,
+//    taking every other K block) issues 4 tcgen05.mma (K = 32 each) per stage
 //    into a fresh TMEM accumulator, so a TMEM buffer holds the FP32 partial of
 //    ONE K block; the 512 TMEM columns hold 512/BN such buffers, so the MMAs
 //    run up to that many K blocks ahead of the promotion;
@@ -44,10 +45,17 @@ constexpr int kEpiThreads = 256;
 constexpr int kMaxGroups = 256;
 constexpr int kTmemCols = 512;
 // Register split: warpgroup 0 shrinks, the two epilogue warpgroups grow.
-// 128 * kRegsLow + 256 * kRegsHigh must not exceed 384 * (registers the
-// kernel is compiled with); the launcher checks that before every launch.
-constexpr int kRegsLow = 72;
-constexpr int kRegsHigh = 216;
+// 128 * kLow + 256 * kHigh must not exceed 384 * (registers the kernel is
+// compiled with); the launcher checks that before every launch. The 128 x 256
+// block-scaled epilogue holds 128 accumulators and two 16-column load buffers
+// per thread, so it takes the larger share.
+template <int BN, bool PER_TENSOR>
+struct RegSplit {
+    static constexpr bool kWide = BN == 256 && !PER_TENSOR;
+    static constexpr int kLow = kWide ? 56 : 72;
+    static constexpr int kHigh = kWide ? 224 : 216;
+    static_assert(128 * kLow + 256 * kHigh <= 384 * 168, "register split exceeds the launch budget");
+};
 
 // Bounded-wait sites reported through the error word.
 enum : unsigned { kSiteProdEmpty = 101, kSiteMmaTmem = 102, kSiteMmaFull = 103, kSiteEpiFull = 104,
@@ -126,6 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         __nv_bfloat16 *__restrict__ y, int M, int N, int K, int groups,
                         const int32_t *__restrict__ offsets, int raster, unsigned *err) {
     using C = Cfg<BN>;
+    constexpr uint32_t kIssuers = PER_TENSOR ? 1u : 2u;  // MMA-issuing lanes
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sA = smem;
@@ -180,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int total = offsets != nullptr ? t_start[groups] : sched.num_m * num_n;
 
     if (warp < 4) {
-        regs_shrink<kRegsLow>();
+        regs_shrink<RegSplit<BN, PER_TENSOR>::kLow>();
         if (warp == 0 && lane == 0) {
             // ------------------------------------------------ TMA producer --
             uint32_t stage = 0, phase = 0;
@@ -206,57 +215,73 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (global_ns() - t0 > kWaitLimitNs) { record_error(err, kErrTimeout, kSiteDrain); break; }
                 }
             }
-        } else if (warp == 1 && lane == 0) {
-            // ------------------------------------------------- MMA issuer --
-            // This lane is the critical path between the epilogue's release of
-            // a TMEM buffer and the next MMAs: it spins (test_wait) rather than
-            // sleeping in try_wait, which shortens every hand-off.
+        } else if ((warp == 1 || (kIssuers == 2 && warp == 2)) && lane == 0) {
+            // ------------------------------------------------ MMA issuers --
+            // tcgen05.mma issue stalls while the tensor pipe is busy, so the
+            // instructions an issuing lane runs between the last MMA of one K
+            // block and the first of the next can leave the pipe idle. In
+            // block-scaled mode every K block has a TMEM buffer of its own, so
+            // two lanes (warps 1 and 2) take alternate K blocks: while one is
+            // stalled feeding the pipe, the other has already waited for its
+            // next buffer and stage. Each lane spins (test_wait), fences once
+            // after both waits, and in block-scaled mode commits only to the
+            // TMEM barrier (the epilogue, which learns from that barrier that
+            // the K block's MMAs are done, frees the shared-memory stage). A
+            // commit tracks the MMAs of the lane that issues it.
             constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
-            uint32_t stage = 0, phase = 0, buf = 0, bphase = 0;
-            uint32_t last_stage = 0, last_phase = 0;
-            bool ok = true, any = false;
+            const uint32_t own = static_cast<uint32_t>(warp - 1);  // K blocks gi with gi % kIssuers == own
+            uint32_t stage = 0, phase = 0, buf = 0, bphase = 0, gi = 0;
+            uint64_t *last_bar = nullptr;
+            uint32_t last_parity = 0;
+            bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                for (int kb = 0; kb < Kg && ok; ++kb) {
-                    if (!PER_TENSOR || kb == 0) {
-                        ok = mbar_wait<true>(&tempty[buf], bphase ^ 1u, abort_flag, err, kSiteMmaTmem);
+                for (int kb = 0; kb < Kg && ok; ++kb, ++gi) {
+                    if (gi % kIssuers == own) {
+                        if (!PER_TENSOR || kb == 0) {
+                            ok = mbar_wait<true>(&tempty[buf], bphase ^ 1u, abort_flag, err, kSiteMmaTmem);
+                            if (!ok) break;
+                        }
+                        ok = mbar_wait<true>(&full[stage], phase, abort_flag, err, kSiteMmaFull);
                         if (!ok) break;
                         tc_fence_after();
-                    }
-                    ok = mbar_wait<true>(&full[stage], phase, abort_flag, err, kSiteMmaFull);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint32_t a0 = smem_u32(sA + stage * C::kABytes);
-                    const uint32_t b0 = smem_u32(sB + stage * C::kBBytes);
-                    const uint32_t d = tmem_base + buf * BN;
+                        const uint32_t a0 = smem_u32(sA + stage * C::kABytes);
+                        const uint32_t b0 = smem_u32(sB + stage * C::kBBytes);
+                        const uint32_t d = tmem_base + buf * BN;
 #pragma unroll
-                    for (int k = 0; k < BK / 32; ++k) {
-                        const uint32_t acc = (k > 0 || (PER_TENSOR && kb > 0)) ? 1u : 0u;
-                        umma_e4m3(d, sdesc_k_sw128(a0 + k * 32), sdesc_k_sw128(b0 + k * 32), idesc, acc);
+                        for (int k = 0; k < BK / 32; ++k) {
+                            const uint32_t acc = (k > 0 || (PER_TENSOR && kb > 0)) ? 1u : 0u;
+                            umma_e4m3(d, sdesc_k_sw128(a0 + k * 32), sdesc_k_sw128(b0 + k * 32), idesc, acc);
+                        }
+                        if (PER_TENSOR) {
+                            umma_commit(&empty[stage]);
+                            last_bar = &empty[stage];
+                            last_parity = phase;
+                        }
+                        if (!PER_TENSOR || kb == Kg - 1) {
+                            umma_commit(&tfull[buf]);
+                            last_bar = &tfull[buf];
+                            last_parity = bphase;
+                        }
                     }
-                    umma_commit(&empty[stage]);
-                    any = true;
-                    last_stage = stage;
-                    last_phase = phase;
                     if (!PER_TENSOR || kb == Kg - 1) {
-                        umma_commit(&tfull[buf]);
                         if (++buf == C::kBufs) { buf = 0; bphase ^= 1u; }
                     }
                     if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
                 }
             }
-            // The last commit arrives once every MMA issued here has finished
-            // reading shared memory and writing TMEM; wait for it before the
-            // CTA frees TMEM (already complete on the normal path).
-            if (any) {
+            // The last commit arrives once every MMA issued by this lane has
+            // finished reading shared memory and writing TMEM; wait for it
+            // before the CTA frees TMEM (already complete on the normal path).
+            if (last_bar != nullptr) {
                 const uint64_t t0 = global_ns();
-                while (!mbar_try_wait(&empty[last_stage], last_phase)) {
+                while (!mbar_try_wait(last_bar, last_parity)) {
                     if (global_ns() - t0 > kWaitLimitNs) { record_error(err, kErrTimeout, kSiteDrain); break; }
                 }
             }
         }
         __syncwarp();  // lanes 1..31 wait for their lane 0
     } else {
-        regs_grow<kRegsHigh>();
+        regs_grow<RegSplit<BN, PER_TENSOR>::kHigh>();
         // ------------------------------------------------------ epilogue --
         const int quarter = warp & 3;      // TMEM lane quarter this warp may access
         const int half = (warp - 4) >> 2;  // which half of the tile's columns
@@ -264,6 +289,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int c0 = half * C::kCols;    // first column within the tile
         const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + c0;
         uint32_t buf = 0, bphase = 0;
+        uint32_t stage = 0;  // shared-memory stage of the current K block (block-scaled mode)
+        const bool frees_stages = (warp == 4 && lane == 0);
         float tensor_scale = 0.0f;
         if (PER_TENSOR) tensor_scale = sa[0] * sw[0];
         bool ok = true;
@@ -294,19 +321,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = __all_sync(0xffffffffu, mbar_wait(&tfull[buf], bphase, abort_flag, err, kSiteEpiFull));
                     if (!ok) break;
                     tc_fence_after();
-                    // 64-column loads (two in flight per wait): two waits per K
-                    // block for BN = 256, one for BN = 128.
+                    // The K block's MMAs are complete, so its operand stage is free.
+                    if (frees_stages) mbar_arrive(&empty[stage]);
+                    if (++stage == C::kStages) stage = 0;
+                    // 16-column chunks, software-pipelined: the load of chunk
+                    // c+1 is in flight while chunk c is promoted. The buffer is
+                    // released as soon as its last chunk is in registers. (The
+                    // small chunks keep the 128-accumulator epilogue free of
+                    // register spills; a spilled, reloaded scale in this loop
+                    // cost a third of the kernel's throughput.)
+                    constexpr int kCh = 16, kN = C::kCols / kCh;
                     const uint32_t base = lane_addr + buf * BN;
+                    uint32_t u[2][kCh];
+                    tmem_ld16_async(base, u[0]);
+                    tmem_wait16(u[0]);
 #pragma unroll
-                    for (int c = 0; c < C::kCols / 64; ++c) {
-                        float p[64];
-                        tmem_ld64(base + c * 64, p);
-                        if (c == C::kCols / 64 - 1) {  // every chunk of this buffer is in registers
+                    for (int c = 0; c < kN; ++c) {
+                        if (c + 1 < kN) {
+                            tmem_ld16_async(base + (c + 1) * kCh, u[(c + 1) & 1]);
+                        } else {
                             tc_fence_before();
                             mbar_arrive(&tempty[buf]);
                         }
 #pragma unroll
-                        for (int j = 0; j < 64; ++j) acc[c * 64 + j] = fmaf(p[j], sc, acc[c * 64 + j]);
+                        for (int j = 0; j < kCh; ++j)
+                            acc[c * kCh + j] = fmaf(__uint_as_float(u[c & 1][j]), sc, acc[c * kCh + j]);
+                        if (c + 1 < kN) tmem_wait16(u[(c + 1) & 1]);
                     }
                     if (++buf == C::kBufs) { buf = 0; bphase ^= 1u; }
                 }
@@ -364,10 +404,11 @@ cudaError_t launch_variant(const void *qa, const float *sa, const void *qw, cons
         cudaError_t e = cudaFuncSetAttribute(gemm_prefill_kernel<BN, PER_TENSOR>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
         // The register re-split inside the kernel needs the launch to hold at
-        // least 128 * kRegsLow + 256 * kRegsHigh registers; refuse otherwise.
+        // least 128 * kLow + 256 * kHigh registers; refuse otherwise.
+        using S = RegSplit<BN, PER_TENSOR>;
         cudaFuncAttributes fa;
         if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, gemm_prefill_kernel<BN, PER_TENSOR>);
-        if (e == cudaSuccess && fa.numRegs * kThreads < 128 * kRegsLow + 256 * kRegsHigh)
+        if (e == cudaSuccess && fa.numRegs * kThreads < 128 * S::kLow + 256 * S::kHigh)
             e = cudaErrorInvalidConfiguration;
         attr_err[device & 63] = e;
     });
