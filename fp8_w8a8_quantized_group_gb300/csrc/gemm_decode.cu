@@ -14,10 +14,14 @@
 //    bytes are in flight per SM with no register staging;
 //  - K is split across the CTAs of a thread-block cluster (up to 8) so that
 //    all CTAs of the grid are resident at once (one wave); each CTA promotes
-//    its K blocks with the scales in FP32 registers, and the partial sums are
-//    reduced through distributed shared memory, each CTA of the cluster
-//    summing (in a fixed order) and storing a slice of the 128 rows. No
-//    global scratch memory is used;
+//    its K blocks with the scales in FP32 registers. Each CTA of the cluster
+//    owns a slice of the 128 rows: every CTA stages its partial sums in its
+//    own shared memory in row order and pushes each rank's slice to that
+//    rank with one bulk copy (counted on an mbarrier there); the owner sums
+//    the slices in a fixed order and stores them. A rank waits only for the
+//    bytes addressed to it and leaves once its own copies have read their
+//    source, so no cluster-wide barrier sits on the critical path and no CTA
+//    is addressed after it exits. No global scratch memory is used;
 //  - launched as a programmatic dependent of the previous kernel in the
 //    stream: before that kernel is known to be complete the CTA only warms
 //    L2 with its first weight tiles (L2 is coherent, so this is safe even if
@@ -37,7 +41,7 @@ namespace {
 constexpr int kRows = 128;      // weight rows per CTA (MMA M)
 constexpr int kTok = 16;        // token slots (MMA N)
 constexpr int BK = 128;
-constexpr int kStages = 6;
+constexpr int kStages = 5;
 constexpr int kWBytes = kRows * BK;
 constexpr int kXBytes = kTok * BK;
 constexpr int kThreads = 256;
@@ -45,10 +49,12 @@ constexpr int kTmemCols = 32;   // two 16-column partial buffers
 constexpr int kL2Warm = 8;      // weight tiles warmed in L2 before the upstream grid completes
 constexpr int kScaleKb = 8;     // K blocks of activation/weight scales staged at a time per epilogue warp
 constexpr int kScaleBytes = 4 * 4 * (kScaleKb * kTok + kScaleKb);
-constexpr int kSmemBytes = 1024 + kStages * (kWBytes + kXBytes) + 8 * (2 * kStages + 4) + 16 + kScaleBytes;
+constexpr int kRecvBytes = kRows * kTok * 4;  // split-K partials addressed to this CTA
+constexpr int kSmemBytes =
+    1024 + kStages * (kWBytes + kXBytes) + kRecvBytes + 8 * (2 * kStages + 5) + 16 + kScaleBytes;
 
 enum : unsigned { kSiteProdEmpty = 201, kSiteMmaTmem = 202, kSiteMmaFull = 203, kSiteEpiFull = 204,
-                  kSiteDrain = 205 };
+                  kSiteDrain = 205, kSiteReduce = 206 };
 
 template <bool PER_TENSOR>
 __global__ void __launch_bounds__(kThreads, 2)
@@ -59,13 +65,14 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sW = smem;
     uint8_t *sX = smem + kStages * kWBytes;
-    uint64_t *full = reinterpret_cast<uint64_t *>(sX + kStages * kXBytes);
+    float *recv = reinterpret_cast<float *>(sX + kStages * kXBytes);  // [splits][rows_per][kTok]
+    uint64_t *full = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(recv) + kRecvBytes);
     uint64_t *empty = full + kStages;
     uint64_t *tfull = empty + kStages;
     uint64_t *tempty = tfull + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
+    uint64_t *rbar = tempty + 2;  // completes when all kRecvBytes have arrived
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(rbar + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    float *red = reinterpret_cast<float *>(sW);  // reused after the main loop
     float *scale_smem = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(tmem_slot) + 16);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -79,8 +86,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
         for (int b = 0; b < 2; ++b) { mbar_init(&tfull[b], 1); mbar_init(&tempty[b], 128); }
+        mbar_init(rbar, 1);
         *abort_flag = 0;
         fence_barrier_init();
+        if (splits > 1) mbar_arrive_expect_tx(rbar, kRecvBytes);
     }
     if (warp == 0 && lane == 0) { tma_prefetch_desc(&tmW); tma_prefetch_desc(&tmX); }
     if (warp == 2) { tmem_alloc(tmem_slot, kTmemCols); tmem_relinquish(); }
@@ -88,6 +97,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // Every CTA's receive barrier is initialised before any rank pushes to it:
+    // each thread passes this cluster barrier before the upstream wait, i.e.
+    // while the previous kernel may still be running.
+    if (splits > 1) cluster_arrive_relaxed();
+    if (splits > 1 && !(warp == 0 && lane == 0)) cluster_wait_acquire();
 
     float acc[kTok];
 #pragma unroll
@@ -99,6 +113,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             // -------------------------------------------------- producer --
             const int warm = (kb1 - kb0) < kL2Warm ? (kb1 - kb0) : kL2Warm;
             for (int i = 0; i < warm; ++i) tma_prefetch_l2_2d(&tmW, (kb0 + i) * BK, n0);
+            if (splits > 1) cluster_wait_acquire();
             grid_dep_wait();
             const uint64_t stream_once = policy_evict_first();
             uint32_t stage = 0, phase = 0;
@@ -239,51 +254,73 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     if (splits > 1) {
         // ------------------------------------- cluster split-K reduction --
-        // Every MMA has completed (the epilogue consumed the last partial, or
-        // the MMA lane drained), so the stage memory can hold the partials.
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncthreads();
+        // Rank q owns rows [q*rows_per, +rows_per). The operand stages are idle
+        // once the last MMA has completed (the epilogue consumed its partial),
+        // so they hold this CTA's partials in row order: rank q's slice is one
+        // contiguous block, copied to [own rank] of q's receive buffer.
+        const uint32_t rank = cluster_ctarank();
+        const int rows_per = kRows / splits;
+        const uint32_t slice_bytes = static_cast<uint32_t>(rows_per * kTok * 4);
+        float *out = reinterpret_cast<float *>(sW);
+        const bool issuer = warp == 4 && lane < splits;  // lane q copies rank q's slice
         if (warp >= 4) {
             const int r = (warp - 4) * 32 + lane;
-            float4 *dst = reinterpret_cast<float4 *>(red + r * kTok);
+            float4 *dst = reinterpret_cast<float4 *>(out + r * kTok);
 #pragma unroll
             for (int j = 0; j < kTok / 4; ++j)
                 dst[j] = make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
-        }
-        cluster_sync_all();
-        // CTA `rank` sums rows [rank*rows_per, +rows_per) over the cluster: one
-        // thread per (row, 4 tokens), 16-byte remote loads from every rank, all
-        // in flight, then a fixed-order sum.
-        const uint32_t rank = cluster_ctarank();
-        const int rows_per = kRows / splits;
-        const int row0 = static_cast<int>(rank) * rows_per;
-        const int quads = (M + 3) / 4;
-        const uint32_t red_addr = smem_u32(red);
-        for (int idx = threadIdx.x; idx < rows_per * quads; idx += kThreads) {
-            const int qd = idx / rows_per;
-            const int row = row0 + (idx - qd * rows_per);
-            const uint32_t off = static_cast<uint32_t>((row * kTok + qd * 4) * 4);
-            float4 part[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-                part[q] = q < splits ? ld_shared_cluster_f32x4(map_shared_rank(red_addr + off, q))
-                                     : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-            float sum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                sum[0] += part[q].x;
-                sum[1] += part[q].y;
-                sum[2] += part[q].z;
-                sum[3] += part[q].w;
-            }
-            const int n = n0 + row;
-            if (n < N) {
-#pragma unroll
-                for (int t = 0; t < 4; ++t)
-                    if (qd * 4 + t < M) y[static_cast<int64_t>(qd * 4 + t) * N + n] = __float2bfloat16_rn(sum[t]);
+            fence_proxy_async_smem();  // the bulk copies read these writes
+            named_bar_sync(1, 128);
+            if (issuer) {
+                const uint32_t q = static_cast<uint32_t>(lane);
+                bulk_copy_to_cluster(map_shared_rank(smem_u32(recv) + rank * slice_bytes, q),
+                                     smem_u32(out) + q * slice_bytes, slice_bytes, map_shared_rank(smem_u32(rbar), q));
+                bulk_commit();
             }
         }
-        cluster_sync_all();
+        // Every rank pushes unconditionally, and a rank that stalls gives up
+        // within one wait limit (the abort flag then short-circuits its other
+        // waits), so this wait - which must not end before the data does, lest
+        // a copy land in a CTA that has exited - takes a longer limit and does
+        // not look at the abort flag.
+        bool got = true;
+        if (threadIdx.x % 32 == 0) {
+            const uint64_t t0 = global_ns();
+            while (!mbar_try_wait(rbar, 0)) {
+                if (global_ns() - t0 > 4 * kWaitLimitNs) {
+                    record_error(err, kErrTimeout, kSiteReduce);
+                    got = false;
+                    break;
+                }
+            }
+        }
+        got = __shfl_sync(0xffffffffu, got, 0) && mbar_try_wait(rbar, 0);
+        if (__all_sync(0xffffffffu, got)) {
+            const int row0 = static_cast<int>(rank) * rows_per;
+            const int quads = (M + 3) / 4;
+            const float4 *rv = reinterpret_cast<const float4 *>(recv);
+            for (int idx = threadIdx.x; idx < rows_per * quads; idx += kThreads) {
+                const int qd = idx / rows_per;
+                const int rl = idx - qd * rows_per;
+                float sum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                for (int src = 0; src < splits; ++src) {  // fixed order: rank 0 first
+                    const float4 v = rv[((src * rows_per + rl) * kTok) / 4 + qd];
+                    sum[0] += v.x;
+                    sum[1] += v.y;
+                    sum[2] += v.z;
+                    sum[3] += v.w;
+                }
+                const int n = n0 + row0 + rl;
+                if (n < N) {
+#pragma unroll
+                    for (int t = 0; t < 4; ++t)
+                        if (qd * 4 + t < M) y[static_cast<int64_t>(qd * 4 + t) * N + n] = __float2bfloat16_rn(sum[t]);
+                }
+            }
+        }
+        // The copies out of this CTA must have read their source before it
+        // exits; everything addressed to it has landed (the wait above).
+        if (issuer) bulk_wait_read();
     }
 
     tc_fence_before();

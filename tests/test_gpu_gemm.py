@@ -279,6 +279,22 @@ def test_block_linear_matches_separate_calls_and_oracle(M, N, K):
         assert_within_tolerance(yg[ms, ns], yo, ab, f"linear {M}x{N}x{K} sampled")
 
 
+def test_block_linear_wide_unsplit_matches_separate_calls():
+    """M <= 16 with N = 19584 (more 128-row blocks than fit twice on the GPU,
+    so K is not split) and K = 8320 (65 K blocks per CTA, more than the ring
+    holds several times over): same codes, scales and Y as the separate calls."""
+    M, N, K = 5, 19584, 8320
+    xd = synth.device_normal_bf16(M, K, 11, "long-k/X", outlier_cols=[7, 4000], outlier_scale=50.0)
+    wd = synth.device_normal_bf16(N, K, 11, "long-k/W", sigma=0.02)
+    qw, sw = ops.quant_weight_block(wd)
+    y, qa, sa = ops.block_linear(xd, qw, sw)
+    qa2, sa2 = ops.quant_act_group(xd)
+    y2 = ops.block_gemm(qa2, sa2, qw, sw)
+    torch.cuda.synchronize()
+    assert torch.equal(qa, qa2) and torch.equal(sa.view(torch.int32), sa2.view(torch.int32))
+    assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
+
+
 def test_block_linear_repeated_calls_stable():
     x, w = synth.block_case(16, 1024, 2048, seed=8)
     xd = to_dev_bf16(x)
