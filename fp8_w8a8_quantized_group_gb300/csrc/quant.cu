@@ -1,10 +1,13 @@
 // Quantizer kernels: BF16 -> E4M3 codes + FP32 scales.
 //
-//  - 1 x 128 activation groups (dynamic, per token): one half-warp per group,
-//    16-byte loads of 8 BF16 per lane, shuffle amax over the half-warp,
-//    8-byte stores of 8 packed codes per lane; launched as a programmatic
-//    dependent so that, in a decode step, its launch overlaps the previous
-//    GEMM and the next GEMM's prologue overlaps it.
+//  - 1 x 128 activation groups (dynamic, per token): four lanes per group,
+//    each with four 16-byte loads of 8 BF16 in flight, a two-step shuffle
+//    amax over the four lanes, one scale per lane and 8-byte stores of 8
+//    packed codes; launched as a programmatic dependent so that, in a decode
+//    step, its launch overlaps the previous GEMM and the next GEMM's prologue
+//    overlaps it. Four lanes per group (rather than sixteen) spread the
+//    per-group work - the shuffle amax and the scale division - over 32
+//    elements per lane.
 //  - 128 x 128 weight blocks: one CTA per block, the block held in registers
 //    between the amax pass and the quantize pass (read once).
 //  - Per tensor: grid-wide amax (atomicMax on the bit pattern of the
@@ -23,45 +26,44 @@ namespace {
 // ------------------------------------------------ 1 x 128 activation groups --
 
 constexpr int kActThreads = 256;
-constexpr int kActRows = kActThreads / 16;          // rows per CTA: one half-warp each
-constexpr int kActUnroll = 4;                       // consecutive groups per half-warp
+constexpr int kActRows = kActThreads / 32;  // rows per CTA: one warp each
+constexpr int kActGroups = 8;               // groups per CTA: one lane quad each
 
-// CTA (blockIdx.x, blockIdx.y) covers rows 16*blockIdx.x .. +15 and groups
-// 4*blockIdx.y .. +3; half-warp h takes row 16*blockIdx.x + h and reads its
-// four groups (1 KB of the row) with four 16-byte loads per lane in flight.
+// CTA (blockIdx.x, blockIdx.y) covers rows 8*blockIdx.x .. +7 (warp w takes
+// row 8*blockIdx.x + w) and groups 8*blockIdx.y .. +7 (lanes 4j..4j+3 take
+// group 8*blockIdx.y + j). Lane c of a quad holds the 16-byte chunks
+// c, c+4, c+8, c+12 of the group's 256 bytes, so each warp-wide load covers
+// 64 contiguous bytes of every group and each store 32.
 __global__ void __launch_bounds__(kActThreads) quant_act_group_kernel(const uint16_t *__restrict__ x,
                                                                       uint8_t *__restrict__ q,
                                                                       float *__restrict__ s, int64_t M,
                                                                       int64_t K) {
     const int64_t Kg = K / 128;
-    const int hw = threadIdx.x >> 4;
-    const int hl = threadIdx.x & 15;
-    const int64_t m = static_cast<int64_t>(blockIdx.x) * kActRows + hw;
-    const int64_t g0 = static_cast<int64_t>(blockIdx.y) * kActUnroll;
+    const int lane = threadIdx.x & 31;
+    const int c = lane & 3;
+    const int64_t m = static_cast<int64_t>(blockIdx.x) * kActRows + (threadIdx.x >> 5);
+    const int64_t g = static_cast<int64_t>(blockIdx.y) * kActGroups + (lane >> 2);
     // Launched as a programmatic dependent: let the next kernel start its
     // prologue, then wait for the kernel that produced x.
     grid_dep_launch();
     grid_dep_wait();
 
-    uint4 v[kActUnroll];
-    const bool row_ok = m < M;
+    const bool ok = m < M && g < Kg;
+    const int64_t base = m * K + g * 128 + c * 8;
+    uint4 v[4];
 #pragma unroll
-    for (int u = 0; u < kActUnroll; ++u) {
-        v[u] = make_uint4(0u, 0u, 0u, 0u);
-        if (row_ok && g0 + u < Kg) v[u] = ld_stream_v4(x + m * K + (g0 + u) * 128 + hl * 8);
+    for (int i = 0; i < 4; ++i) {
+        v[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (ok) v[i] = ld_stream_v4(x + base + 32 * i);
     }
+    float a = fmaxf(fmaxf(amax8(v[0]), amax8(v[1])), fmaxf(amax8(v[2]), amax8(v[3])));
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+    if (ok) {
+        const float sc = block_scale(a);
 #pragma unroll
-    for (int u = 0; u < kActUnroll; ++u) {
-        float a = amax8(v[u]);
-        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 8));
-        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
-        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
-        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-        if (row_ok && g0 + u < Kg) {
-            const float sc = block_scale(a);
-            *reinterpret_cast<uint2 *>(q + m * K + (g0 + u) * 128 + hl * 8) = quant8(v[u], sc);
-            if (hl == 0) s[(g0 + u) * M + m] = sc;
-        }
+        for (int i = 0; i < 4; ++i) *reinterpret_cast<uint2 *>(q + base + 32 * i) = quant8(v[i], sc);
+        if (c == 0) s[g * M + m] = sc;
     }
 }
 
@@ -196,7 +198,7 @@ cudaError_t launch_quant_act_group(const void *x, void *q, float *s, int64_t M, 
                                    const DeviceInfo &dev, cudaStream_t stream) {
     (void)dev;
     const int64_t rows = (M + kActRows - 1) / kActRows;
-    const int64_t cols = (K / 128 + kActUnroll - 1) / kActUnroll;
+    const int64_t cols = (K / 128 + kActGroups - 1) / kActGroups;
     if (rows == 0 || cols == 0) return cudaSuccess;
     if (rows > 0x7FFFFFFF || cols > 65535) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
