@@ -29,12 +29,16 @@ constexpr int kActThreads = 256;
 constexpr int kActRows = kActThreads / 32;  // rows per CTA: one warp each
 constexpr int kActGroups = 8;               // groups per CTA: one lane quad each
 
+// Bounded to six resident CTAs per SM (at most 40 registers): at the default
+// 55 registers only four fit and the kernel is latency-bound (8192 x 14336:
+// 62.5 us at six, 68.7 us at four).
+//
 // CTA (blockIdx.x, blockIdx.y) covers rows 8*blockIdx.x .. +7 (warp w takes
 // row 8*blockIdx.x + w) and groups 8*blockIdx.y .. +7 (lanes 4j..4j+3 take
 // group 8*blockIdx.y + j). Lane c of a quad holds the 16-byte chunks
 // c, c+4, c+8, c+12 of the group's 256 bytes, so each warp-wide load covers
 // 64 contiguous bytes of every group and each store 32.
-__global__ void __launch_bounds__(kActThreads) quant_act_group_kernel(const uint16_t *__restrict__ x,
+__global__ void __launch_bounds__(kActThreads, 6) quant_act_group_kernel(const uint16_t *__restrict__ x,
                                                                       uint8_t *__restrict__ q,
                                                                       float *__restrict__ s, int64_t M,
                                                                       int64_t K) {
