@@ -75,6 +75,7 @@ __global__ void __launch_bounds__(kActThreads, 6) quant_act_group_kernel(const u
 
 constexpr int kWThreads = 256;
 constexpr int kWChunks = 128 * 16 / kWThreads;  // 16-byte chunks per thread (8)
+constexpr int kWRowsPerPass = kWThreads / 16;
 
 // Block (nb, kb) = (blockIdx.y, blockIdx.x). Chunk c = t + 256 j covers row
 // c / 16 of the block and bytes 16 (c % 16) .. of the row's 256-byte span.
@@ -90,7 +91,7 @@ __global__ void __launch_bounds__(kWThreads) quant_weight_block_kernel(const uin
     float a = 0.0f;
 #pragma unroll
     for (int j = 0; j < kWChunks; ++j) {
-        const int64_t row = nb * 128 + (t >> 4) + 16 * j;
+        const int64_t row = nb * 128 + (t >> 4) + kWRowsPerPass * j;
         v[j] = make_uint4(0u, 0u, 0u, 0u);
         if (row < N) v[j] = ld_stream_v4(w + row * K + kb * 128 + col);
     }
@@ -106,7 +107,7 @@ __global__ void __launch_bounds__(kWThreads) quant_weight_block_kernel(const uin
     const float sc = block_scale(a);
 #pragma unroll
     for (int j = 0; j < kWChunks; ++j) {
-        const int64_t row = nb * 128 + (t >> 4) + 16 * j;
+        const int64_t row = nb * 128 + (t >> 4) + kWRowsPerPass * j;
         if (row < N) *reinterpret_cast<uint2 *>(q + row * K + kb * 128 + col) = quant8(v[j], sc);
     }
     if (t == 0) s[nb * Kg + kb] = sc;
@@ -134,6 +135,7 @@ __device__ __forceinline__ float block_reduce_max(float a, float *scratch) {
 __global__ void __launch_bounds__(kTThreads) tensor_amax_kernel(const uint16_t *__restrict__ x, int64_t n8,
                                                                 unsigned *__restrict__ amax_bits) {
     __shared__ float scratch[kTThreads / 32];
+    grid_dep_launch();  // the quantize pass may be scheduled; it waits for this grid
     float a = 0.0f;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kTThreads;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * kTThreads + threadIdx.x; i < n8; i += stride * kTUnroll) {
@@ -155,6 +157,10 @@ __global__ void __launch_bounds__(kTThreads) tensor_amax_kernel(const uint16_t *
 __global__ void __launch_bounds__(kTThreads) tensor_quant_kernel(const uint16_t *__restrict__ x,
                                                                  uint8_t *__restrict__ q, int64_t n8,
                                                                  const float *scale, int from_amax) {
+    // Launched as a programmatic dependent of the amax pass (or of whatever
+    // precedes a static call): wait for it before reading the scale or x.
+    grid_dep_launch();
+    grid_dep_wait();
     const float stored = *scale;
     const float sc = from_amax ? block_scale(stored) : stored;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kTThreads;
@@ -173,9 +179,34 @@ __global__ void __launch_bounds__(kTThreads) tensor_quant_kernel(const uint16_t 
     }
 }
 
-// *scale: amax bit pattern -> scale.
+// *scale: amax bit pattern -> scale, once every CTA of the quantize pass
+// (a programmatic predecessor) has read it.
 __global__ void tensor_scale_finalize_kernel(float *scale) {
+    grid_dep_wait();
     *scale = block_scale(*scale);
+}
+
+// Grid of one resident wave for `kernel` at kTThreads threads.
+template <typename Kernel>
+int64_t tensor_grid(Kernel kernel, int64_t want, const DeviceInfo &dev) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kTThreads, 0) != cudaSuccess || per_sm < 1)
+        per_sm = 1;
+    const int64_t cap = static_cast<int64_t>(dev.sm_count) * per_sm;
+    return want < cap ? want : cap;
+}
+
+cudaError_t launch_pdl(const void *fn, unsigned grid, unsigned block, void **args, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
 // Whole per-tensor quantization in one CTA (small tensors).
@@ -244,21 +275,27 @@ cudaError_t launch_quant_per_tensor(const void *x, void *q, float *scale, int64_
         tensor_quant_small_kernel<<<1, 1024, 0, stream>>>(xp, qp, n8, scale, is_static ? 1 : 0);
         return cudaGetLastError();
     }
-    const int64_t want = (n8 + kTThreads * kTUnroll - 1) / (kTThreads * kTUnroll);
-    const int64_t cap = static_cast<int64_t>(dev.sm_count) * 8;
-    const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
+    // Each pass runs as one resident wave, and the quantize and finalize
+    // kernels are programmatic dependents of their predecessors, so their
+    // launches overlap the previous pass.
+    static const int64_t kWant = kTThreads * kTUnroll;
+    const int64_t want = (n8 + kWant - 1) / kWant;
     if (!is_static) {
         cudaError_t e = cudaMemsetAsync(scale, 0, sizeof(float), stream);
         if (e != cudaSuccess) return e;
-        tensor_amax_kernel<<<grid, kTThreads, 0, stream>>>(xp, n8, reinterpret_cast<unsigned *>(scale));
+        const unsigned ga = static_cast<unsigned>(tensor_grid(tensor_amax_kernel, want, dev));
+        tensor_amax_kernel<<<ga, kTThreads, 0, stream>>>(xp, n8, reinterpret_cast<unsigned *>(scale));
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    tensor_quant_kernel<<<grid, kTThreads, 0, stream>>>(xp, qp, n8, scale, is_static ? 0 : 1);
-    cudaError_t e = cudaGetLastError();
+    const unsigned gq = static_cast<unsigned>(tensor_grid(tensor_quant_kernel, want, dev));
+    int from_amax = is_static ? 0 : 1;
+    const float *cscale = scale;
+    void *qargs[] = {&xp, &qp, const_cast<int64_t *>(&n8), &cscale, &from_amax};
+    cudaError_t e = launch_pdl(reinterpret_cast<const void *>(tensor_quant_kernel), gq, kTThreads, qargs, stream);
     if (e != cudaSuccess || is_static) return e;
-    tensor_scale_finalize_kernel<<<1, 1, 0, stream>>>(scale);
-    return cudaGetLastError();
+    void *fargs[] = {&scale};
+    return launch_pdl(reinterpret_cast<const void *>(tensor_scale_finalize_kernel), 1, 1, fargs, stream);
 }
 
 }  // namespace fp8k
