@@ -11,8 +11,14 @@
 //  - 128 x 128 weight blocks: one CTA per block, the block held in registers
 //    between the amax pass and the quantize pass (read once).
 //  - Per tensor: grid-wide amax (atomicMax on the bit pattern of the
-//    non-negative amax, kept in the output scale slot), then quantize; a
+//    non-negative amax, kept in the output scale slot), then quantize, each
+//    pass one resident wave of CTAs over equal contiguous slices; a
 //    single-CTA kernel does both for small tensors.
+//
+// The weight-block and per-tensor quantize passes are bound by instruction
+// issue; they reach the correctly rounded quotient's code through one
+// reciprocal per block or tensor (quant8_recip below), with a division only
+// near rounding boundaries. Codes are identical to quant8's either way.
 //
 // Every scale is fl32(max(amax, 1e-10) / 448) and every code
 // e4m3(fl32(x / scale)); "[vLLM] FP8" page, sections "스케일링 전략 체계"
@@ -22,6 +28,48 @@
 
 namespace fp8k {
 namespace {
+
+// The E4M3 code pair of two FP32 values (low byte = a): the hardware's
+// round-to-nearest-even, saturating conversion.
+__device__ __forceinline__ uint32_t e4m3_pair(float a, float b) {
+    return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
+}
+
+// Same codes as quant8(v, s) - those of the correctly rounded quotients
+// RN(x/s) - for kernels bound by instruction issue, with r = RN(1/s)
+// computed once by the caller. q = RN(x*r) carries two roundings, so it lies
+// within 1.5 * 2^-23 |q| of RN(x/s), while RN(q * (1 -+ 2^-21)) lie more than
+// 3.5 * 2^-23 |q| away on either side: RN(x/s) lies between them. Rounding to
+// nearest even and saturating is monotonic, so when both bounds convert to
+// the codes of q, so does RN(x/s). Otherwise (near a rounding boundary of the
+// conversion), and whenever r overflows (s zero or subnormal, where x*r
+// could be 0 * Inf), the chunk takes correctly rounded divisions.
+__device__ __forceinline__ uint2 quant8_recip(const uint4 &v, float s, float r) {
+    const float x[8] = {bf16lo(v.x), bf16hi(v.x), bf16lo(v.y), bf16hi(v.y),
+                        bf16lo(v.z), bf16hi(v.z), bf16lo(v.w), bf16hi(v.w)};
+    constexpr float kDown = 1.0f - 0x1p-21f, kUp = 1.0f + 0x1p-21f;  // both exact in FP32
+    float q[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] = __fmul_rn(x[i], r);
+    uint2 out, lo, hi;
+    out.x = e4m3_pair(q[0], q[1]) | (e4m3_pair(q[2], q[3]) << 16);
+    out.y = e4m3_pair(q[4], q[5]) | (e4m3_pair(q[6], q[7]) << 16);
+    lo.x = e4m3_pair(__fmul_rn(q[0], kDown), __fmul_rn(q[1], kDown)) |
+           (e4m3_pair(__fmul_rn(q[2], kDown), __fmul_rn(q[3], kDown)) << 16);
+    lo.y = e4m3_pair(__fmul_rn(q[4], kDown), __fmul_rn(q[5], kDown)) |
+           (e4m3_pair(__fmul_rn(q[6], kDown), __fmul_rn(q[7], kDown)) << 16);
+    hi.x = e4m3_pair(__fmul_rn(q[0], kUp), __fmul_rn(q[1], kUp)) |
+           (e4m3_pair(__fmul_rn(q[2], kUp), __fmul_rn(q[3], kUp)) << 16);
+    hi.y = e4m3_pair(__fmul_rn(q[4], kUp), __fmul_rn(q[5], kUp)) |
+           (e4m3_pair(__fmul_rn(q[6], kUp), __fmul_rn(q[7], kUp)) << 16);
+    if ((lo.x != out.x) | (lo.y != out.y) | (hi.x != out.x) | (hi.y != out.y) | (fabsf(r) == INFINITY)) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) q[i] = __fdiv_rn(x[i], s);
+        out.x = e4m3_pair(q[0], q[1]) | (e4m3_pair(q[2], q[3]) << 16);
+        out.y = e4m3_pair(q[4], q[5]) | (e4m3_pair(q[6], q[7]) << 16);
+    }
+    return out;
+}
 
 // ------------------------------------------------ 1 x 128 activation groups --
 
@@ -105,10 +153,11 @@ __global__ void __launch_bounds__(kWThreads) quant_weight_block_kernel(const uin
 #pragma unroll
     for (int i = 1; i < kWThreads / 32; ++i) a = fmaxf(a, warp_amax[i]);
     const float sc = block_scale(a);
+    const float rc = __frcp_rn(sc);
 #pragma unroll
     for (int j = 0; j < kWChunks; ++j) {
         const int64_t row = nb * 128 + (t >> 4) + kWRowsPerPass * j;
-        if (row < N) *reinterpret_cast<uint2 *>(q + row * K + kb * 128 + col) = quant8(v[j], sc);
+        if (row < N) *reinterpret_cast<uint2 *>(q + row * K + kb * 128 + col) = quant8_recip(v[j], sc, rc);
     }
     if (t == 0) s[nb * Kg + kb] = sc;
 }
@@ -137,13 +186,13 @@ __global__ void __launch_bounds__(kTThreads) tensor_amax_kernel(const uint16_t *
     __shared__ float scratch[kTThreads / 32];
     grid_dep_launch();  // the quantize pass may be scheduled; it waits for this grid
     float a = 0.0f;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * kTThreads;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kTThreads + threadIdx.x; i < n8; i += stride * kTUnroll) {
+    const int64_t c0 = n8 * blockIdx.x / gridDim.x, c1 = n8 * (blockIdx.x + 1) / gridDim.x;
+    for (int64_t i = c0 + threadIdx.x; i < c1; i += kTThreads * kTUnroll) {
         uint4 v[kTUnroll];
 #pragma unroll
         for (int u = 0; u < kTUnroll; ++u) {
-            const int64_t j = i + u * stride;
-            v[u] = j < n8 ? ld_stream_v4(x + j * 8) : make_uint4(0u, 0u, 0u, 0u);
+            const int64_t j = i + u * kTThreads;
+            v[u] = j < c1 ? ld_stream_v4(x + j * 8) : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
         for (int u = 0; u < kTUnroll; ++u) a = fmaxf(a, amax8(v[u]));
@@ -163,18 +212,19 @@ __global__ void __launch_bounds__(kTThreads) tensor_quant_kernel(const uint16_t 
     grid_dep_wait();
     const float stored = *scale;
     const float sc = from_amax ? block_scale(stored) : stored;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * kTThreads;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kTThreads + threadIdx.x; i < n8; i += stride * kTUnroll) {
+    const float rc = __frcp_rn(sc);
+    const int64_t c0 = n8 * blockIdx.x / gridDim.x, c1 = n8 * (blockIdx.x + 1) / gridDim.x;
+    for (int64_t i = c0 + threadIdx.x; i < c1; i += kTThreads * kTUnroll) {
         uint4 v[kTUnroll];
 #pragma unroll
         for (int u = 0; u < kTUnroll; ++u) {
-            const int64_t j = i + u * stride;
-            v[u] = j < n8 ? ld_stream_v4(x + j * 8) : make_uint4(0u, 0u, 0u, 0u);
+            const int64_t j = i + u * kTThreads;
+            v[u] = j < c1 ? ld_stream_v4(x + j * 8) : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
         for (int u = 0; u < kTUnroll; ++u) {
-            const int64_t j = i + u * stride;
-            if (j < n8) *reinterpret_cast<uint2 *>(q + j * 8) = quant8(v[u], sc);
+            const int64_t j = i + u * kTThreads;
+            if (j < c1) *reinterpret_cast<uint2 *>(q + j * 8) = quant8_recip(v[u], sc, rc);
         }
     }
 }
