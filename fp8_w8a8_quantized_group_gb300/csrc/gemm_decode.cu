@@ -23,10 +23,11 @@
 //    source, so no cluster-wide barrier sits on the critical path and no CTA
 //    is addressed after it exits. No global scratch memory is used;
 //  - launched as a programmatic dependent of the previous kernel in the
-//    stream: before that kernel is known to be complete the CTA only warms
-//    L2 with its first weight tiles (L2 is coherent, so this is safe even if
-//    the previous kernel writes the weights); every shared-memory load and
-//    every global write comes after griddepcontrol.wait.
+//    stream: before that kernel is known to be complete the CTA already
+//    loads its first weight tiles into their stages and warms L2 with the
+//    next few (weights are not written by any kernel that triggers this one
+//    early); the activation codes and scales are read, and every global
+//    write is made, after griddepcontrol.wait.
 //
 // Block mode applies Sw[n/128][kb] * Sa[kb][m] per K block; per-tensor mode
 // accumulates all of the CTA's K range in TMEM and applies sa * sw once.
@@ -46,7 +47,7 @@ constexpr int kWBytes = kRows * BK;
 constexpr int kXBytes = kTok * BK;
 constexpr int kThreads = 256;
 constexpr int kTmemCols = 32;   // two 16-column partial buffers
-constexpr int kL2Warm = 8;      // weight tiles warmed in L2 before the upstream grid completes
+constexpr int kL2Warm = 12;     // weight tiles loaded or warmed in L2 before the upstream grid completes
 constexpr int kScaleKb = 8;     // K blocks of activation/weight scales staged at a time per epilogue warp
 constexpr int kScaleBytes = 4 * 4 * (kScaleKb * kTok + kScaleKb);
 constexpr int kRecvBytes = kRows * kTok * 4;  // split-K partials addressed to this CTA
@@ -111,14 +112,25 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (warp == 0) {
         if (lane == 0) {
             // -------------------------------------------------- producer --
-            const int warm = (kb1 - kb0) < kL2Warm ? (kb1 - kb0) : kL2Warm;
-            for (int i = 0; i < warm; ++i) tma_prefetch_l2_2d(&tmW, (kb0 + i) * BK, n0);
+            // Weights are read before the upstream wait (the caller's contract:
+            // no kernel that triggers this one early writes them): the first
+            // kStages weight tiles go straight into their stages, the next
+            // few are warmed in L2. Activation codes come after the wait.
+            const uint64_t stream_once = policy_evict_first();
+            const int nkb = kb1 - kb0;
+            const int pre = nkb < kStages ? nkb : kStages;
+            for (int i = 0; i < pre; ++i) {
+                mbar_arrive_expect_tx(&full[i], kWBytes + kXBytes);
+                tma_load_2d_hint(sW + i * kWBytes, &tmW, &full[i], (kb0 + i) * BK, n0, stream_once);
+            }
+            const int warm = nkb < kL2Warm ? nkb : kL2Warm;
+            for (int i = pre; i < warm; ++i) tma_prefetch_l2_2d(&tmW, (kb0 + i) * BK, n0);
             if (splits > 1) cluster_wait_acquire();
             grid_dep_wait();
-            const uint64_t stream_once = policy_evict_first();
-            uint32_t stage = 0, phase = 0;
-            int issued = 0;
-            for (int kb = kb0; kb < kb1; ++kb) {
+            for (int i = 0; i < pre; ++i) tma_load_2d(sX + i * kXBytes, &tmX, &full[i], (kb0 + i) * BK, 0);
+            uint32_t stage = static_cast<uint32_t>(pre % kStages), phase = pre == kStages ? 1u : 0u;
+            int issued = pre;
+            for (int kb = kb0 + pre; kb < kb1; ++kb) {
                 if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err, kSiteProdEmpty)) break;
                 mbar_arrive_expect_tx(&full[stage], kWBytes + kXBytes);
                 tma_load_2d_hint(sW + stage * kWBytes, &tmW, &full[stage], kb * BK, n0, stream_once);

@@ -134,7 +134,11 @@ int fp8_quant_per_tensor(const void *x_bf16, void *q_e4m3, float *scale,
  *   written. Offsets are read on the device and are trusted.
  *   num_groups in [1, FP8_MAX_GROUPS].
  * M <= 16 (dense) uses the weight-streaming decode kernel, otherwise the
- * tile-persistent prefill kernel.
+ * tile-persistent prefill kernel. The decode kernel is a programmatic
+ * dependent of the work before it on `stream` and starts reading qw before
+ * that work has completed: qw must not be written by a kernel that allows
+ * its dependents to launch early (griddepcontrol.launch_dependents).
+ * fp8_quant_weight_block never does; a plain stream order suffices.
  * Errors: NULL, SHAPE, ALIGN, UNSUPPORTED, ARG, DEVICE, CUDA.
  */
 int fp8_block_gemm(const void *qa, const float *sa, const void *qw, const float *sw,
@@ -149,6 +153,8 @@ int fp8_block_gemm(const void *qa, const float *sa, const void *qw, const float 
  *   qa [M][K] E4M3, qw [N][K] E4M3, y [M][N] BF16.
  *   sa, sw: ONE FP32 each, in DEVICE memory (as written by fp8_quant_per_tensor).
  *   K and N positive multiples of 16, M >= 0.
+ * M <= 16 uses the decode kernel, with the same condition on qw as
+ * fp8_block_gemm.
  * Errors: NULL, SHAPE, ALIGN, DEVICE, CUDA.
  */
 int fp8_tensor_gemm(const void *qa, const float *sa, const void *qw, const float *sw,
@@ -168,7 +174,7 @@ int fp8_tensor_gemm(const void *qa, const float *sa, const void *qw, const float
  * Two launches on `stream`: the quantization kernel, then the decode
  * (M <= 16) or prefill GEMM. The quantization kernel is a programmatic
  * dependent of the work before it, and the GEMM of the quantization kernel:
- * each starts its prologue (and the decode GEMM warms L2 with its weights)
+ * each starts its prologue (and the decode GEMM loads its first weights)
  * while its predecessor finishes, and waits for it before reading its output.
  * Errors: NULL, SHAPE, ALIGN, DEVICE, CUDA.
  */
