@@ -560,6 +560,11 @@ def oracle_decode_sample(budget_s: float):
     return nbytes / t_total / 1e9, desc, t_total
 
 
+def decode_workload() -> str:
+    return (f"decode block-scaled W8A8: M in {DECODE_M} x projections {SHAPES} x {LAYERS} "
+            "layers of distinct weights; step = act quant + GEMM for each")
+
+
 def reference_arm(args):
     """--impl reference: the CPU oracle as it stands, on the decode workload."""
     rank = int(os.environ.get("RANK", "0"))
@@ -576,8 +581,8 @@ def reference_arm(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded SplitMix64/Box-Muller)",
-            "config": {"workload": "decode block-scaled W8A8 (M=1 sample of the four Llama-8B-like projections)",
-                       "parallelism": "none (host)"},
+            "config": {"workload": decode_workload(), "parallelism": "host, one thread",
+                       "sample": "each step a bounded sample of the workload (cpu_baseline.sample)"},
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
@@ -735,8 +740,7 @@ def main():
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3xe4m3->f32 (bf16 in/out)",
         "data": "synthetic (seeded; normal activations with 0.1% x50 outlier channels, N(0,0.02) weights)",
-        "config": {"workload": f"decode block-scaled W8A8: M in {DECODE_M} x projections {SHAPES} x {LAYERS} "
-                               "layers of distinct weights; step = act quant + GEMM for each",
+        "config": {"workload": decode_workload(),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": f"inputs larger than L2: {LAYERS} layers of FP8 weights "
                          f"({sum(N * K for N, K in SHAPES) * LAYERS / 1e9:.2f} GB) stream once per M per step",
