@@ -208,6 +208,12 @@ const char *fp8_status_string(int status) {
     }
 }
 
+int fp8_selftest_bounded_wait(void *stream) {
+    const fp8k::DeviceInfo *dev = nullptr;
+    if (int st = fp8k::current_device(&dev)) return st;
+    return fp8k::to_status(fp8k::launch_selftest_wait(*dev, static_cast<cudaStream_t>(stream)));
+}
+
 int fp8_device_error(void *stream, int *out_code, int *out_site) {
     if (!out_code) return FP8_ERR_NULL;
     const fp8k::DeviceInfo *dev = nullptr;

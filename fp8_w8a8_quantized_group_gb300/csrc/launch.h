@@ -38,4 +38,8 @@ cudaError_t launch_gemm_decode(const void *qa, const float *sa, const void *qw, 
                                int64_t M, int64_t N, int64_t K, bool per_tensor, const DeviceInfo &dev,
                                cudaStream_t stream);
 
+// One CTA whose waits never complete: the first gives up after the wait limit
+// and records FP8_ERR_TIMEOUT (site 901); the second returns at the abort flag.
+cudaError_t launch_selftest_wait(const DeviceInfo &dev, cudaStream_t stream);
+
 }  // namespace fp8k

@@ -109,6 +109,11 @@ def fp8_status_string(status: int) -> str:
     return _lib.load().fp8_status_string(status).decode()
 
 
+def fp8_selftest_bounded_wait(stream=None) -> None:
+    """Launch the bounded-wait self-test kernel (about one second on the device)."""
+    _check(_lib.load().fp8_selftest_bounded_wait(_stream(stream)), "fp8_selftest_bounded_wait")
+
+
 def fp8_device_error(stream=None) -> tuple[int, int]:
     """Synchronise the stream and read-and-clear the device error word: (status, site)."""
     code = ctypes.c_int(0)

@@ -193,6 +193,23 @@ const char *fp8_status_string(int status);
  */
 int fp8_device_error(void *stream, int *out_code, int *out_site);
 
+/*
+ * Self-test of the bounded device waits (a test hook, not part of the
+ * computation). Launches on `stream` one CTA of the same wait machinery the
+ * GEMM kernels use, with waits that can never complete:
+ *  - one thread waits on an mbarrier that nobody arrives at; after the wait
+ *    limit (about one second) it records FP8_ERR_TIMEOUT with site 901 in
+ *    the device error word and raises the CTA's abort flag;
+ *  - a second thread starts its own such wait half a limit later and returns
+ *    as soon as it sees the flag, without recording (site 902 would show a
+ *    failure to stop).
+ * Nothing faults or hangs: the kernel ends about one second after it starts,
+ * and the context stays usable. A following fp8_device_error reports
+ * FP8_ERR_TIMEOUT and site 901 (and clears them).
+ * Errors: DEVICE, CUDA.
+ */
+int fp8_selftest_bounded_wait(void *stream);
+
 #ifdef __cplusplus
 }
 #endif

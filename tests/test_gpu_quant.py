@@ -91,11 +91,13 @@ def test_per_tensor_static_weights():
     assert s.item() == float(so)  # a static scale is left unchanged
 
 
-@pytest.mark.parametrize("scale", [1.0, 3.0, 0.1, 2.0 ** -20, 1e-30, 7.0e10])
+@pytest.mark.parametrize("scale", [1.0, 3.0, 0.1, 2.0 ** -20, 1e-30, 7.0e10, 1e-40, 3e38])
 def test_every_bf16_pattern_through_static_quantization(scale):
     """All 65536 BF16 bit patterns through the static per-tensor quantizer:
     pins the device division and E4M3 conversion (rounding, saturation,
-    subnormals, signed zero, infinities) to the oracle's codec."""
+    subnormals, signed zero, infinities) to the oracle's codec. 1e-40 is a
+    subnormal scale (its reciprocal overflows: the exact-division fallback),
+    3e38 one whose reciprocal is subnormal."""
     x = np.arange(65536, dtype=np.uint32).astype(np.uint16).reshape(4096, 16)
     sc = np.float32(scale)
     q, _ = ops.quant_per_tensor(to_dev_bf16(x), scale=torch.tensor([sc], device="cuda"))
