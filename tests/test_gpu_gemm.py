@@ -54,6 +54,10 @@ def _sample_points(M, N, n_random=4096, seed=0):
     (1, 256, 256), (4, 384, 1024), (7, 512, 512), (16, 1024, 2048), (3, 272, 384),
     (17, 256, 256),     # smallest prefill-kernel case, ragged
     (129, 384, 512), (300, 272, 1024), (256, 256, 128),
+    # decode, unsplit (153 row blocks): a K range of exactly the ring depth
+    # (every stage loaded before the upstream wait) and one block more (the
+    # first refill after those)
+    (16, 19584, 640), (5, 19584, 768),
 ])
 def test_block_gemm_full_compare(M, N, K):
     if (M, N, K) == (16, 256, 256):
