@@ -1,0 +1,103 @@
+"""Host-side logic of bench.py (no GPU): the algorithmic byte counts the
+metric divides by, the staleness guard on the committed ncu traffic ratios,
+and the reference arm's JSON line."""
+import hashlib
+import io
+import json
+import os
+import types
+from contextlib import redirect_stdout
+
+import numpy as np
+import pytest
+
+import bench
+
+
+def _layout_bytes(M, N, K):
+    """Bytes of the buffers one block-scaled GEMM reads and writes, from arrays
+    shaped as the C ABI lays them out."""
+    qa = np.empty((M, K), np.uint8)
+    sa = np.empty((K // 128, M), np.float32)
+    qw = np.empty((N, K), np.uint8)
+    sw = np.empty((-(-N // 128), K // 128), np.float32)
+    y = np.empty((M, N), np.uint16)  # BF16
+    return qa.nbytes + sa.nbytes + qw.nbytes + sw.nbytes + y.nbytes
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 4096, 4096), (16, 28672, 4096), (4, 272, 14336), (16, 6144, 4096)])
+def test_gemm_bytes_are_the_buffers_it_touches(M, N, K):
+    assert bench.gemm_bytes(M, N, K) == _layout_bytes(M, N, K)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 4096, 4096), (16, 4096, 14336)])
+def test_linear_bytes_add_the_bf16_input(M, N, K):
+    x = np.empty((M, K), np.uint16)
+    assert bench.linear_bytes(M, N, K) == _layout_bytes(M, N, K) + x.nbytes
+
+
+def test_act_quant_bytes():
+    M, K = 8192, 14336
+    x = np.empty((M, K), np.uint16)
+    q = np.empty((M, K), np.uint8)
+    s = np.empty((K // 128, M), np.float32)
+    assert bench.act_quant_bytes(M, K) == x.nbytes + q.nbytes + s.nbytes
+
+
+def _fake_root(tmp_path, ratio=1.25):
+    src = tmp_path / "kernel.cu"
+    src.write_text("// a kernel\n")
+    sha = hashlib.sha256(src.read_bytes()).hexdigest()
+    (tmp_path / "profiles").mkdir()
+    entry = {"k": {"sources": ["kernel.cu"], "sha256": sha,
+                   "captures": {"a": {"dram_bytes": 125, "algorithmic_bytes": 100, "ratio": ratio},
+                                "b": {"dram_bytes": 75, "algorithmic_bytes": 100, "ratio": 0.75}}}}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(entry))
+    return src
+
+
+def test_traffic_uses_the_mean_captured_ratio(tmp_path, monkeypatch):
+    _fake_root(tmp_path)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench._traffic("k", 1000.0) == pytest.approx(1000.0)  # mean of 1.25 and 0.75
+
+
+def test_traffic_is_null_once_the_source_changed(tmp_path, monkeypatch):
+    src = _fake_root(tmp_path)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    src.write_text("// a kernel, edited after the capture\n")
+    assert bench._traffic("k", 1000.0) is None
+    assert bench._traffic("unknown_kernel", 1000.0) is None
+
+
+def test_committed_traffic_hashes_match_the_sources():
+    """Every committed capture is of the kernel sources as they are now."""
+    with open(os.path.join(bench.ROOT, "profiles", "traffic.json")) as f:
+        entries = json.load(f)
+    for name, e in entries.items():
+        d = hashlib.sha256()
+        for s in e["sources"]:
+            with open(os.path.join(bench.ROOT, s), "rb") as f:
+                d.update(f.read())
+        assert d.hexdigest() == e["sha256"], f"{name}: sources changed since its ncu capture"
+
+
+def test_reference_arm_line(monkeypatch):
+    monkeypatch.setattr(bench, "oracle_decode_sample", lambda budget: (0.25, "a sample", 0.1))
+    args = types.SimpleNamespace(gpus=1, steps=2, warmup=3)
+    out = io.StringIO()
+    with redirect_stdout(out):
+        bench.reference_arm(args)
+    line = json.loads(out.getvalue().strip().splitlines()[-1])
+    assert line["impl"] == "reference"
+    assert line["metric"] == bench.METRIC and line["unit"] == "GB/s" and line["higher_is_better"] is True
+    assert line["value"] == 0.25 and line["steps"] == 2 and line["warmup"] == 3
+    assert line["config"]["workload"] == bench.decode_workload()
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["sample"] == "a sample"
+    assert line["e2e"] == {"value": 0.25, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_oracle_sample_runs_on_a_tiny_budget():
+    gbps, desc, seconds = bench.oracle_decode_sample(0.001)
+    assert gbps > 0 and seconds > 0
+    assert "[128, 128, 128, 128]" in desc  # the smallest sample: one 128-column block per projection
