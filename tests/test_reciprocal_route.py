@@ -1,0 +1,87 @@
+"""The reciprocal route of the weight-block and per-tensor quantizers, checked
+as mathematics on the host (the GPU tests check the kernels themselves).
+
+For a scale s and a value x the kernels take q = RN(x * RN(1/s)) and accept
+its E4M3 code when RN(q * (1 - 2^-21)) and RN(q * (1 + 2^-21)) convert to the
+same code; otherwise they divide. The claim: an accepted code always equals
+the code of the correctly rounded quotient RN(x/s). numpy's float32
+arithmetic is IEEE round-to-nearest-even with subnormals, so it reproduces
+every rounding step; the E4M3 conversion is round-to-nearest-even with
+saturation, here torch's cast of the value clipped to +-448 (the oracle's
+encoder is pinned to that cast within the range). Every BF16 value is tried
+against scales over the whole FP32 range, subnormal and largest included,
+and against scales that put x/s next to a rounding midpoint.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+
+E4M3_MAX = np.float32(448.0)
+DOWN = np.float32(1.0 - 2.0 ** -21)
+UP = np.float32(1.0 + 2.0 ** -21)
+
+
+def _codes(v: np.ndarray) -> np.ndarray:
+    t = torch.from_numpy(np.clip(v, -E4M3_MAX, E4M3_MAX))
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def _all_bf16_values() -> np.ndarray:
+    x = synth.bf16_bits_to_f32(np.arange(65536, dtype=np.uint32).astype(np.uint16))
+    return x[~np.isnan(x)].astype(np.float32)
+
+
+def _scales() -> list[float]:
+    rng = np.random.default_rng(2024)
+    out = list(np.exp2(rng.uniform(-149.0, 127.99, 300)).astype(np.float32))
+    out += [np.float32(v) for v in (1.4e-45, 1e-40, 2.0 ** -126, 1e-10 / 448, 1.0, 3.0, 0.1, 448.0, 3e38,
+                                    3.4028235e38)]
+    # scales that put x/s a few ulps from the midpoint between two E4M3 codes
+    vals = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    mids = (vals[:0x7E] + vals[1:0x7F]) / 2
+    for _ in range(40):
+        x = float(_all_bf16_values()[rng.integers(0, 65000)])
+        if x == 0 or not np.isfinite(x):
+            continue
+        s = np.float32(abs(x) / rng.choice(mids[8:]))
+        for k in (-2, -1, 0, 1, 2):
+            out.append(np.float32(s + np.float32(k) * np.spacing(s)))
+    return [float(v) for v in out if np.isfinite(v) and v > 0]
+
+
+SCALES = _scales()
+
+
+@pytest.mark.parametrize("chunk", range(4))
+def test_accepted_codes_equal_the_divided_codes(chunk):
+    x = _all_bf16_values()
+    accepted_total = 0
+    for s in SCALES[chunk::4]:
+        s = np.float32(s)
+        with np.errstate(over="ignore", invalid="ignore", divide="ignore", under="ignore"):
+            r = np.float32(1.0) / s
+            exact = x / s
+            q = x * r
+            lo, hi = q * DOWN, q * UP
+        if not np.isfinite(r):
+            continue  # the kernels divide for every element
+        cq = _codes(q)
+        accept = (_codes(lo) == cq) & (_codes(hi) == cq)
+        bad = accept & (cq != _codes(exact))
+        assert not bad.any(), f"s={s!r}: x={x[bad][:4]} accepted with a code other than the division's"
+        accepted_total += int(accept.sum())
+    assert accepted_total > 0
+
+
+def test_most_values_take_the_fast_path_at_typical_scales():
+    """At scales of ordinary weights and activations nearly every element is
+    accepted, so the division stays rare."""
+    x = synth.bf16_bits_to_f32(synth.to_bf16(np.random.default_rng(5).normal(0.0, 1.0, 65536)))
+    s = np.float32(np.abs(x).max() / 448.0)
+    r = np.float32(1.0) / s
+    q = (x * r).astype(np.float32)
+    cq = _codes(q)
+    accept = (_codes(q * DOWN) == cq) & (_codes(q * UP) == cq)
+    assert accept.mean() > 0.99
