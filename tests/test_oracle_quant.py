@@ -197,6 +197,25 @@ def test_special_cases_reduce(oracle_lib):
     assert np.array_equal(q_s, q_t)
 
 
+@pytest.mark.parametrize("where", ["first", "last", "interior"])
+@pytest.mark.parametrize("sign", [1.0, -1.0])
+def test_per_tensor_scale_sees_every_element(oracle_lib, where, sign):
+    """The dynamic per-tensor scale is RN32(amax/448) over the whole tensor: a
+    single largest element, wherever it lies and whatever its sign, sets it."""
+    x = synth.weights(9, 48, seed=31, label="pt-amax", sigma=0.02)
+    n = x.size
+    pos = {"first": 0, "last": n - 1, "interior": n // 2 + 7}[where]
+    flat = x.ravel().copy()
+    big = synth.to_bf16(np.array([sign * 3.0625]))[0]  # exact in BF16, far above N(0, 0.02^2)
+    flat[pos] = big
+    xt = flat.reshape(x.shape)
+    q, s = oracle_lib.quant_per_tensor(xt)
+    assert s == _f32_exact(Fraction(3.0625) / 448)
+    assert q.ravel()[pos] == (0xFE if sign < 0 else 0x7E)
+    q_b, s_b = oracle_lib.quant_blocks(xt, 9, 48, "rows_major")
+    assert s_b[0, 0] == s and np.array_equal(q_b, q)
+
+
 def test_ragged_last_block(oracle_lib):
     w = synth.weights(130, 256, seed=2, label="rag")
     q, s = oracle_lib.quant_weight_block(w, 128, 128)
