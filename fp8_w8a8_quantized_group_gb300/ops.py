@@ -35,16 +35,47 @@ def _check(status: int, where: str):
         raise Fp8Error(status, where)
 
 
-def _ptr(t: torch.Tensor | None, dtype: torch.dtype | None = None, what: str = "tensor"):
+CODES = (torch.uint8, torch.float8_e4m3fn)  # E4M3 codes: either dtype, the same bytes
+
+
+def _need(t: torch.Tensor | None, n: int, what: str) -> None:
+    """The entry point reads or writes n elements of t: refuse a smaller buffer
+    (the C ABI sees only a pointer and could not tell)."""
+    if t is not None and t.numel() < n:
+        raise ValueError(f"{what}: has {t.numel()} elements, the call uses {n}")
+
+
+def _cdiv(a: int, b: int) -> int:
+    return -(-a // b) if b > 0 else 0
+
+
+def _dtype(t: torch.Tensor | None, dtype, what: str) -> None:
+    dtypes = dtype if isinstance(dtype, tuple) else (dtype,)
+    if t is not None and t.dtype not in dtypes:
+        raise TypeError(f"{what}: expected {' or '.join(map(str, dtypes))}, got {t.dtype}")
+
+
+def _ptr(t: torch.Tensor | None, what: str, device: int | None):
     if t is None:
         return None
-    if dtype is not None and t.dtype != dtype:
-        raise TypeError(f"{what}: expected {dtype}, got {t.dtype}")
     if not t.is_cuda:
         raise ValueError(f"{what}: must be a CUDA tensor")
+    if t.device.index != device:
+        raise ValueError(f"{what}: on {t.device}, but the current device is cuda:{device}")
     if not t.is_contiguous():
         raise ValueError(f"{what}: must be contiguous")
     return t.data_ptr() if t.numel() else None
+
+
+def _ptrs(*specs):
+    """Pointers of (tensor, dtype, name) triples: dtypes checked first, then
+    that each tensor is contiguous on the current CUDA device."""
+    for t, dtype, what in specs:
+        _dtype(t, dtype, what)
+    device = None
+    if any(t is not None and t.is_cuda for t, _, _ in specs):
+        device = torch.cuda.current_device()
+    return [_ptr(t, what, device) for t, _, what in specs]
 
 
 def _stream(stream) -> int | None:
@@ -54,55 +85,77 @@ def _stream(stream) -> int | None:
 
 
 # ---------------------------------------------------------- C ABI mirror ---
+#
+# Each function first checks that every buffer holds at least the elements the
+# entry point touches for the sizes it is given (M, K from the input's shape,
+# N from the output's), then passes the pointers.
 
 def fp8_quant_act_group(x, q, scales, group_k: int = GROUP, stream=None) -> None:
     M, K = x.shape
-    _check(_lib.load().fp8_quant_act_group(_ptr(x, torch.bfloat16, "x"), _ptr(q, torch.uint8, "q"),
-                                           _ptr(scales, torch.float32, "scales"), M, K, group_k,
-                                           _stream(stream)), "fp8_quant_act_group")
+    _need(q, M * K, "q")
+    _need(scales, (K // group_k if group_k > 0 else 0) * M, "scales")
+    args = _ptrs((x, torch.bfloat16, "x"), (q, CODES, "q"), (scales, torch.float32, "scales"))
+    _check(_lib.load().fp8_quant_act_group(*args, M, K, group_k, _stream(stream)), "fp8_quant_act_group")
 
 
 def fp8_quant_weight_block(w, q, scales, block_n: int = GROUP, block_k: int = GROUP, stream=None) -> None:
     N, K = w.shape
-    _check(_lib.load().fp8_quant_weight_block(_ptr(w, torch.bfloat16, "w"), _ptr(q, torch.uint8, "q"),
-                                              _ptr(scales, torch.float32, "scales"), N, K, block_n, block_k,
-                                              _stream(stream)), "fp8_quant_weight_block")
+    _need(q, N * K, "q")
+    _need(scales, _cdiv(N, block_n) * (K // block_k if block_k > 0 else 0), "scales")
+    args = _ptrs((w, torch.bfloat16, "w"), (q, CODES, "q"), (scales, torch.float32, "scales"))
+    _check(_lib.load().fp8_quant_weight_block(*args, N, K, block_n, block_k, _stream(stream)),
+           "fp8_quant_weight_block")
 
 
 def fp8_quant_per_tensor(x, q, scale, is_static: bool, stream=None) -> None:
     rows, cols = x.shape
-    _check(_lib.load().fp8_quant_per_tensor(_ptr(x, torch.bfloat16, "x"), _ptr(q, torch.uint8, "q"),
-                                            _ptr(scale, torch.float32, "scale"), rows, cols,
-                                            1 if is_static else 0, _stream(stream)), "fp8_quant_per_tensor")
+    _need(q, rows * cols, "q")
+    _need(scale, 1, "scale")
+    args = _ptrs((x, torch.bfloat16, "x"), (q, CODES, "q"), (scale, torch.float32, "scale"))
+    _check(_lib.load().fp8_quant_per_tensor(*args, rows, cols, 1 if is_static else 0, _stream(stream)),
+           "fp8_quant_per_tensor")
 
 
 def fp8_block_gemm(qa, sa, qw, sw, y, block_n: int = GROUP, block_k: int = GROUP, group_k: int = GROUP,
                    num_groups: int = 1, group_offsets=None, stream=None) -> None:
     M, K = qa.shape
     N = y.shape[1]
-    _check(_lib.load().fp8_block_gemm(_ptr(qa, torch.uint8, "qa"), _ptr(sa, torch.float32, "sa"),
-                                      _ptr(qw, torch.uint8, "qw"), _ptr(sw, torch.float32, "sw"),
-                                      _ptr(y, torch.bfloat16, "y"), M, N, K, block_n, block_k, group_k,
-                                      num_groups, _ptr(group_offsets, torch.int32, "group_offsets"),
+    G = max(num_groups, 1)
+    _need(sa, _cdiv(K, group_k) * M, "sa")
+    _need(qw, G * N * K, "qw")
+    _need(sw, G * _cdiv(N, block_n) * _cdiv(K, block_k), "sw")
+    _need(y, M * N, "y")
+    _need(group_offsets, G + 1, "group_offsets")
+    *args, offsets = _ptrs((qa, CODES, "qa"), (sa, torch.float32, "sa"), (qw, CODES, "qw"),
+                           (sw, torch.float32, "sw"), (y, torch.bfloat16, "y"),
+                           (group_offsets, torch.int32, "group_offsets"))
+    _check(_lib.load().fp8_block_gemm(*args, M, N, K, block_n, block_k, group_k, num_groups, offsets,
                                       _stream(stream)), "fp8_block_gemm")
 
 
 def fp8_tensor_gemm(qa, sa, qw, sw, y, stream=None) -> None:
     M, K = qa.shape
     N = y.shape[1]
-    _check(_lib.load().fp8_tensor_gemm(_ptr(qa, torch.uint8, "qa"), _ptr(sa, torch.float32, "sa"),
-                                       _ptr(qw, torch.uint8, "qw"), _ptr(sw, torch.float32, "sw"),
-                                       _ptr(y, torch.bfloat16, "y"), M, N, K, _stream(stream)),
-           "fp8_tensor_gemm")
+    _need(sa, 1, "sa")
+    _need(qw, N * K, "qw")
+    _need(sw, 1, "sw")
+    _need(y, M * N, "y")
+    args = _ptrs((qa, CODES, "qa"), (sa, torch.float32, "sa"), (qw, CODES, "qw"), (sw, torch.float32, "sw"),
+                 (y, torch.bfloat16, "y"))
+    _check(_lib.load().fp8_tensor_gemm(*args, M, N, K, _stream(stream)), "fp8_tensor_gemm")
 
 
 def fp8_block_linear(x, qa, sa, qw, sw, y, stream=None) -> None:
     M, K = x.shape
     N = y.shape[1]
-    _check(_lib.load().fp8_block_linear(_ptr(x, torch.bfloat16, "x"), _ptr(qa, torch.uint8, "qa"),
-                                        _ptr(sa, torch.float32, "sa"), _ptr(qw, torch.uint8, "qw"),
-                                        _ptr(sw, torch.float32, "sw"), _ptr(y, torch.bfloat16, "y"), M, N, K,
-                                        _stream(stream)), "fp8_block_linear")
+    _need(qa, M * K, "qa")
+    _need(sa, _cdiv(K, GROUP) * M, "sa")
+    _need(qw, N * K, "qw")
+    _need(sw, _cdiv(N, GROUP) * _cdiv(K, GROUP), "sw")
+    _need(y, M * N, "y")
+    args = _ptrs((x, torch.bfloat16, "x"), (qa, CODES, "qa"), (sa, torch.float32, "sa"), (qw, CODES, "qw"),
+                 (sw, torch.float32, "sw"), (y, torch.bfloat16, "y"))
+    _check(_lib.load().fp8_block_linear(*args, M, N, K, _stream(stream)), "fp8_block_linear")
 
 
 def fp8_status_string(status: int) -> str:
