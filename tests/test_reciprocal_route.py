@@ -54,25 +54,44 @@ def _scales() -> list[float]:
 SCALES = _scales()
 
 
-@pytest.mark.parametrize("chunk", range(4))
-def test_accepted_codes_equal_the_divided_codes(chunk):
+def _accepted_and_wrong(scales, down, up):
+    """(accepted, accepted with a code other than the division's, an example)."""
     x = _all_bf16_values()
-    accepted_total = 0
-    for s in SCALES[chunk::4]:
+    accepted = wrong = 0
+    example = None
+    for s in scales:
         s = np.float32(s)
         with np.errstate(over="ignore", invalid="ignore", divide="ignore", under="ignore"):
             r = np.float32(1.0) / s
             exact = x / s
             q = x * r
-            lo, hi = q * DOWN, q * UP
+            lo, hi = q * down, q * up
         if not np.isfinite(r):
             continue  # the kernels divide for every element
         cq = _codes(q)
         accept = (_codes(lo) == cq) & (_codes(hi) == cq)
         bad = accept & (cq != _codes(exact))
-        assert not bad.any(), f"s={s!r}: x={x[bad][:4]} accepted with a code other than the division's"
-        accepted_total += int(accept.sum())
-    assert accepted_total > 0
+        accepted += int(accept.sum())
+        wrong += int(bad.sum())
+        if bad.any() and example is None:
+            example = (s, x[bad][:4])
+    return accepted, wrong, example
+
+
+@pytest.mark.parametrize("chunk", range(4))
+def test_accepted_codes_equal_the_divided_codes(chunk):
+    accepted, wrong, example = _accepted_and_wrong(SCALES[chunk::4], DOWN, UP)
+    assert wrong == 0, f"s, x = {example}: accepted with a code other than the division's"
+    assert accepted > 0
+
+
+def test_a_bracket_too_narrow_to_move_q_is_caught():
+    """The check has teeth: with bounds RN(q (1 -+ 2^-25)), which round back to
+    q itself, every element is accepted, and the same enumeration finds
+    accepted codes that differ from the division's."""
+    narrow_down, narrow_up = np.float32(1.0 - 2.0 ** -25), np.float32(1.0 + 2.0 ** -25)
+    _, wrong, _ = _accepted_and_wrong(SCALES[::4], narrow_down, narrow_up)
+    assert wrong > 0
 
 
 def test_most_values_take_the_fast_path_at_typical_scales():
