@@ -123,3 +123,21 @@ def test_python_binding_names_match_header():
     import fp8_w8a8_quantized_group_gb300 as pkg
     for name in _lib.header_functions():
         assert callable(getattr(pkg, name)), name
+
+
+def test_header_compiles_as_c_and_links(lib, tmp_path):
+    """A C11 client (tests/abi_client.c) compiles against include/fp8w8a8.h
+    with gcc in pedantic mode, with no C++ or CUDA header, links the library
+    and gets the expected statuses for calls that are refused on the host."""
+    import os
+    import subprocess
+
+    here = os.path.dirname(os.path.abspath(__file__))
+    exe = str(tmp_path / "abi_client")
+    libdir = os.path.dirname(_lib.LIB_PATH)
+    subprocess.run(["gcc", "-std=c11", "-pedantic", "-Wall", "-Wextra", "-Werror",
+                    "-I", os.path.dirname(_lib.HEADER), os.path.join(here, "abi_client.c"), "-o", exe,
+                    "-L", libdir, "-lfp8w8a8", f"-Wl,-rpath,{libdir}"], check=True)
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.strip().endswith("checks passed")
