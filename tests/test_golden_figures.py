@@ -4,7 +4,6 @@ from the oracle's quantized layout and from the byte and FLOP model the
 benchmark divides by."""
 import os
 
-import numpy as np
 import pytest
 
 import bench
