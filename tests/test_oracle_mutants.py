@@ -86,6 +86,16 @@ MUTANTS = [
     ("grouped: weight scales of expert 0 for every expert", "sw + expert * nb_count * kb_count", "sw"),
     ("per-tensor gemm: activation scale dropped", "double a = (double)sa * ora_e4m3_decode(qa[m * K + k]);",
      "double a = ora_e4m3_decode(qa[m * K + k]);"),
+    ("per-tensor gemm: weight scale dropped", "double b = (double)sw * ora_e4m3_decode(qw[n * K + k]);",
+     "double b = ora_e4m3_decode(qw[n * K + k]);"),
+    ("points: rows paired with another point's column", "qw, sw, K, gk, bn, bk, ms[i], ns[i],",
+     "qw, sw, K, gk, bn, bk, ms[i], ns[npts - 1 - i],"),
+    ("per-tensor points: weight row of another point", "qa + ms[i] * K, sa, qw + ns[i] * K, sw,",
+     "qa + ms[i] * K, sa, qw + ns[npts - 1 - i] * K, sw,"),
+    ("grouped: expert 0's weights for every expert", "qw + expert * N * K", "qw"),
+    ("static quantization: scale taken as its reciprocal",
+     "q[i] = quant_value(bf16_bits_to_float(x[i]), scale);",
+     "q[i] = quant_value(bf16_bits_to_float(x[i]), 1.0f / scale);"),
 ]
 
 
