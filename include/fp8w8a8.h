@@ -34,6 +34,10 @@
  *  - The return value is a status (FP8_OK = 0). Argument errors are detected
  *    on the host before anything is enqueued. A zero M (or rows) is a valid
  *    no-op.
+ *  - The quantizers by group and block, the GEMMs and fp8_block_linear take
+ *    each of M, N, K (and N * num_groups when grouped) up to INT_MAX; larger
+ *    values give FP8_ERR_SHAPE. fp8_quant_per_tensor takes any rows * cols
+ *    that fits in half of the int64_t range.
  *  - Device-side waits in the kernels are bounded (about one second); if one
  *    expires the kernel stops early and records FP8_ERR_TIMEOUT, which
  *    fp8_device_error() reports. Kernels never trap.
@@ -188,8 +192,10 @@ const char *fp8_status_string(int status);
  * Synchronises `stream`, then reads and clears the current device's error
  * word, which kernels set when a bounded wait expires. *out_code receives
  * FP8_OK or FP8_ERR_TIMEOUT; *out_site (may be NULL) a number naming the wait
- * that expired. Returns FP8_OK, or FP8_ERR_CUDA if the synchronisation or the
- * read failed (e.g. an earlier kernel faulted).
+ * that expired. Returns FP8_OK; FP8_ERR_NULL if out_code is NULL (checked
+ * first, on the host); FP8_ERR_DEVICE if the current device is not sm_103;
+ * FP8_ERR_CUDA if the synchronisation or the read failed (e.g. an earlier
+ * kernel faulted).
  */
 int fp8_device_error(void *stream, int *out_code, int *out_site);
 

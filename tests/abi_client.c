@@ -82,8 +82,21 @@ int main(void)
     EXPECT(fp8_block_linear(FAKE, FAKE, FAKE_F, FAKE, FAKE_F, FAKE, 4, 256, 200, NULL), FP8_ERR_SHAPE);
     EXPECT(fp8_block_linear(FAKE, FAKE, FAKE_F, FAKE, FAKE_F, NULL, 4, 256, 256, NULL), FP8_ERR_NULL);
 
-    /* status text: one non-empty string per status, and one for unknown values */
+    /* dimensions past the documented limits */
+    EXPECT(fp8_quant_act_group(FAKE, FAKE, FAKE_F, (int64_t)1 << 31, 256, FP8_GROUP, NULL), FP8_ERR_SHAPE);
+    EXPECT(fp8_quant_weight_block(FAKE, FAKE, FAKE_F, (int64_t)1 << 31, 256, FP8_GROUP, FP8_GROUP, NULL),
+           FP8_ERR_SHAPE);
+    EXPECT(fp8_quant_per_tensor(FAKE, FAKE, FAKE_F, (int64_t)1 << 62, 16, 0, NULL), FP8_ERR_SHAPE);
+    EXPECT(fp8_block_gemm(FAKE, FAKE_F, FAKE, FAKE_F, FAKE, 64, (int64_t)1 << 24, 256, FP8_GROUP, FP8_GROUP,
+                          FP8_GROUP, FP8_MAX_GROUPS, (const int32_t *)FAKE, NULL),
+           FP8_ERR_SHAPE); /* N * num_groups = 2^32 */
+    EXPECT(fp8_tensor_gemm(FAKE, FAKE_F, FAKE, FAKE_F, FAKE, 4, 256, ((int64_t)1 << 31) + 16, NULL), FP8_ERR_SHAPE);
+    EXPECT(fp8_block_linear(FAKE, FAKE, FAKE_F, FAKE, FAKE_F, FAKE, 4, (int64_t)1 << 31, 256, NULL), FP8_ERR_SHAPE);
+
+    /* the error word needs somewhere to go */
     EXPECT(fp8_device_error(NULL, NULL, NULL), FP8_ERR_NULL);
+
+    /* status text: one non-empty string per status, and one for unknown values */
     for (s = FP8_OK; s <= FP8_ERR_TIMEOUT + 1; ++s) {
         const char *text = fp8_status_string(s);
         ++n_checks;

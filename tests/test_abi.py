@@ -138,6 +138,12 @@ def test_header_compiles_as_c_and_links(lib, tmp_path):
     subprocess.run(["gcc", "-std=c11", "-pedantic", "-Wall", "-Wextra", "-Werror",
                     "-I", os.path.dirname(_lib.HEADER), os.path.join(here, "abi_client.c"), "-o", exe,
                     "-L", libdir, "-lfp8w8a8", f"-Wl,-rpath,{libdir}"], check=True)
+    import torch
+    if torch.cuda.is_available():
+        # The client passes fake device addresses that only the host checks
+        # keep from being used; it is not run where a regression of those
+        # checks could launch a kernel on them.
+        pytest.skip("compiled and linked; run only where no GPU is visible")
     r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
     assert r.returncode == 0, r.stderr
     assert r.stdout.strip().endswith("checks passed")
