@@ -560,6 +560,22 @@ def oracle_decode_sample(budget_s: float):
     return nbytes / t_total / 1e9, desc, t_total
 
 
+def host_cpu() -> dict:
+    """The host the CPU baseline ran on: logical CPUs, architecture and, where
+    the platform reports it, the CPU model."""
+    import platform
+    model = ""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return {"logical_cpus": os.cpu_count(), "machine": platform.machine(), "model": model}
+
+
 def decode_workload() -> str:
     return (f"decode block-scaled W8A8: M in {DECODE_M} x projections {SHAPES} x {LAYERS} "
             "layers of distinct weights; step = act quant + GEMM for each")
@@ -583,7 +599,8 @@ def reference_arm(args):
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded SplitMix64/Box-Muller)",
             "config": {"workload": decode_workload(), "parallelism": "host, one thread",
                        "sample": "each step a bounded sample of the workload (cpu_baseline.sample)"},
-            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc,
+                             "host": host_cpu()},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
 
@@ -734,7 +751,7 @@ def main():
     if world == 1:
         v, desc, secs = oracle_decode_sample(args.cpu_budget)
         cpu = {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc,
-               "seconds": round(secs, 2)}
+               "seconds": round(secs, 2), "host": host_cpu()}
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",

@@ -97,6 +97,8 @@ def test_reference_arm_line(monkeypatch):
     assert line["config"]["workload"] == bench.decode_workload()
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["sample"] == "a sample"
     assert line["e2e"] == {"value": 0.25, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    host = line["cpu_baseline"]["host"]
+    assert host["logical_cpus"] == os.cpu_count() and host["machine"] and isinstance(host["model"], str)
 
 
 def test_oracle_sample_runs_on_a_tiny_budget():
