@@ -13,6 +13,7 @@ from .ops import (  # noqa: F401
     fp8_block_linear,
     fp8_device_error,
     fp8_selftest_bounded_wait,
+    fp8_selftest_encode_f32,
     fp8_quant_act_group,
     fp8_quant_per_tensor,
     fp8_quant_weight_block,

@@ -30,6 +30,7 @@ SIGNATURES = {
     "fp8_status_string": ([I32], ctypes.c_char_p),
     "fp8_device_error": ([P, ctypes.POINTER(I32), ctypes.POINTER(I32)], I32),
     "fp8_selftest_bounded_wait": ([P], I32),
+    "fp8_selftest_encode_f32": ([ctypes.c_uint32, I64, P, P], I32),
 }
 
 STATUS = {0: "FP8_OK", 1: "FP8_ERR_NULL", 2: "FP8_ERR_SHAPE", 3: "FP8_ERR_ALIGN", 4: "FP8_ERR_UNSUPPORTED",

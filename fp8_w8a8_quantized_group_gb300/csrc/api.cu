@@ -214,6 +214,18 @@ int fp8_selftest_bounded_wait(void *stream) {
     return fp8k::to_status(fp8k::launch_selftest_wait(*dev, static_cast<cudaStream_t>(stream)));
 }
 
+int fp8_selftest_encode_f32(uint32_t first_bits, int64_t n, void *out_e4m3, void *stream) {
+    if (n < 0 || n % 8 != 0) return FP8_ERR_SHAPE;
+    if (static_cast<uint64_t>(first_bits) + static_cast<uint64_t>(n) > (uint64_t(1) << 32)) return FP8_ERR_SHAPE;
+    if (n == 0) return FP8_OK;
+    if (!out_e4m3) return FP8_ERR_NULL;
+    if (misaligned(out_e4m3, 16)) return FP8_ERR_ALIGN;
+    const fp8k::DeviceInfo *dev = nullptr;
+    if (int st = fp8k::current_device(&dev)) return st;
+    return fp8k::to_status(
+        fp8k::launch_selftest_encode(first_bits, n, out_e4m3, *dev, static_cast<cudaStream_t>(stream)));
+}
+
 int fp8_device_error(void *stream, int *out_code, int *out_site) {
     if (!out_code) return FP8_ERR_NULL;
     const fp8k::DeviceInfo *dev = nullptr;

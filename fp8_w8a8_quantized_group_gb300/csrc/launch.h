@@ -42,4 +42,9 @@ cudaError_t launch_gemm_decode(const void *qa, const float *sa, const void *qw, 
 // and records FP8_ERR_TIMEOUT (site 901); the second returns at the abort flag.
 cudaError_t launch_selftest_wait(const DeviceInfo &dev, cudaStream_t stream);
 
+// The hardware E4M3 conversion of the n FP32 values with bit patterns first,
+// first + 1, ... into out (n a multiple of 8, first + n <= 2^32).
+cudaError_t launch_selftest_encode(uint32_t first, int64_t n, void *out, const DeviceInfo &dev,
+                                   cudaStream_t stream);
+
 }  // namespace fp8k

@@ -167,6 +167,14 @@ def fp8_selftest_bounded_wait(stream=None) -> None:
     _check(_lib.load().fp8_selftest_bounded_wait(_stream(stream)), "fp8_selftest_bounded_wait")
 
 
+def fp8_selftest_encode_f32(first_bits: int, out, stream=None) -> None:
+    """Hardware E4M3 codes of the FP32 values with bit patterns first_bits,
+    first_bits + 1, ... into out (one per element; numel a multiple of 8)."""
+    (ptr,) = _ptrs((out, CODES, "out"))
+    _check(_lib.load().fp8_selftest_encode_f32(first_bits, out.numel(), ptr, _stream(stream)),
+           "fp8_selftest_encode_f32")
+
+
 def fp8_device_error(stream=None) -> tuple[int, int]:
     """Synchronise the stream and read-and-clear the device error word: (status, site)."""
     code = ctypes.c_int(0)

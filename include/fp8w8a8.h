@@ -216,6 +216,20 @@ int fp8_device_error(void *stream, int *out_code, int *out_site);
  */
 int fp8_selftest_bounded_wait(void *stream);
 
+/*
+ * Self-test of the E4M3 conversion (a test hook, not part of the computation).
+ * Writes to out_e4m3[i], for 0 <= i < n, the code of the FP32 value whose bit
+ * pattern is first_bits + i, by the same hardware conversion the quantizers
+ * apply to their quotients (round to nearest even, saturating to +-448).
+ * Sweeping all 2^32 patterns compares that conversion with an independent
+ * encoder on every FP32 value.
+ *
+ *   out_e4m3  [n] bytes of DEVICE memory, output, 16-byte aligned.
+ *   n         a multiple of 8, with first_bits + n <= 2^32.
+ * Errors: NULL, SHAPE, ALIGN, DEVICE, CUDA.
+ */
+int fp8_selftest_encode_f32(uint32_t first_bits, int64_t n, void *out_e4m3, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

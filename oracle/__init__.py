@@ -56,6 +56,8 @@ def _load():
         lib.ora_e4m3_decode.restype = ctypes.c_double
         lib.ora_e4m3_encode.argtypes = [F]
         lib.ora_e4m3_encode.restype = ctypes.c_uint8
+        lib.ora_e4m3_encode_bits.argtypes = [ctypes.c_uint32, I, P]
+        lib.ora_e4m3_encode_bits.restype = None
         lib.ora_quant_blocks.argtypes = [P, I, I, I, I, P, P, I, I]
         lib.ora_quant_blocks.restype = None
         lib.ora_quant_static.argtypes = [P, I, F, P]
@@ -101,6 +103,20 @@ def e4m3_decode(code: int) -> float:
 def e4m3_encode(v: float) -> int:
     """E4M3 code of an FP32 value: RNE, saturating to +-448, signed zero kept."""
     return int(_load().ora_e4m3_encode(float(np.float32(v))))
+
+
+def e4m3_encode_bits(first: int, n: int, out: np.ndarray | None = None) -> np.ndarray:
+    """Codes of the n FP32 values with bit patterns first, first + 1, ...
+    (first + n <= 2**32), written into out (uint8, contiguous) if given."""
+    if not (0 <= first and n >= 0 and first + n <= 1 << 32):
+        raise ValueError("bit range outside the 32-bit patterns")
+    if out is None:
+        out = np.empty(n, dtype=np.uint8)
+    if out.dtype != np.uint8 or out.size != n or not out.flags["C_CONTIGUOUS"]:
+        raise ValueError("out must be a contiguous uint8 array of n elements")
+    if n:
+        _load().ora_e4m3_encode_bits(first, n, _ptr(out))
+    return out
 
 
 def e4m3_decode_array(codes: np.ndarray) -> np.ndarray:

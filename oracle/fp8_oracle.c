@@ -109,6 +109,18 @@ uint8_t ora_e4m3_encode(float v)
     return sign | e4m3_code_of_exact(r);
 }
 
+/* Codes of the n FP32 values whose bit patterns are first, first+1, ...:
+ * the encoder above applied to each (for sweeps over the whole FP32 range). */
+void ora_e4m3_encode_bits(uint32_t first, int64_t n, uint8_t *out)
+{
+    int64_t i;
+    for (i = 0; i < n; i++) {
+        union { uint32_t u; float f; } cv;
+        cv.u = first + (uint32_t)i;
+        out[i] = ora_e4m3_encode(cv.f);
+    }
+}
+
 /* -------------------------------------------------------------- inputs --- */
 
 /* BF16 bit pattern -> FP32 value (exact: BF16 is the top half of FP32). */

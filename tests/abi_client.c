@@ -93,6 +93,14 @@ int main(void)
     EXPECT(fp8_tensor_gemm(FAKE, FAKE_F, FAKE, FAKE_F, FAKE, 4, 256, ((int64_t)1 << 31) + 16, NULL), FP8_ERR_SHAPE);
     EXPECT(fp8_block_linear(FAKE, FAKE, FAKE_F, FAKE, FAKE_F, FAKE, 4, (int64_t)1 << 31, 256, NULL), FP8_ERR_SHAPE);
 
+    /* the conversion self-test: n a multiple of 8, no pattern past 0xFFFFFFFF */
+    EXPECT(fp8_selftest_encode_f32(0, 12, FAKE, NULL), FP8_ERR_SHAPE);
+    EXPECT(fp8_selftest_encode_f32(0, -8, FAKE, NULL), FP8_ERR_SHAPE);
+    EXPECT(fp8_selftest_encode_f32(0xFFFFFFF8u, 16, FAKE, NULL), FP8_ERR_SHAPE);
+    EXPECT(fp8_selftest_encode_f32(0, 8, NULL, NULL), FP8_ERR_NULL);
+    EXPECT(fp8_selftest_encode_f32(0, 8, ODD8, NULL), FP8_ERR_ALIGN);
+    EXPECT(fp8_selftest_encode_f32(0xFFFFFFF8u, 0, NULL, NULL), FP8_OK);
+
     /* the error word needs somewhere to go */
     EXPECT(fp8_device_error(NULL, NULL, NULL), FP8_ERR_NULL);
 

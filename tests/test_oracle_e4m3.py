@@ -177,3 +177,21 @@ def test_signed_zero_and_underflow(oracle_lib):
     assert oracle_lib.e4m3_encode(2.0 ** -10) == 0x00
     assert oracle_lib.e4m3_encode(float(np.nextafter(np.float32(2.0 ** -10), np.float32(1)))) == 0x01
     assert oracle_lib.e4m3_encode(float("nan")) & 0x7F == 0x7F
+
+
+@pytest.mark.parametrize("first,n", [(0, 4096), (0x3F7FF000, 8192), (0x43DFF000, 8192), (0x7F7FFF00, 0x100),
+                                     (0x7F800000 - 8, 16), (0x80000000, 4096), (0xC3E00000 - 64, 128),
+                                     (0xFFFFFFFF - 15, 16)])
+def test_bulk_encoder_is_the_per_value_encoder(oracle_lib, first, n):
+    """The range encoder used for sweeps over all FP32 patterns gives, for every
+    pattern, the code of the per-value encoder (pinned above), including the
+    last pattern 0xFFFFFFFF and ranges across +-448, +-Inf and NaN."""
+    bits = (np.arange(n, dtype=np.uint64) + first).astype(np.uint32)
+    vals = bits.view(np.float32)
+    got = oracle_lib.e4m3_encode_bits(first, n)
+    assert np.array_equal(got, oracle_lib.e4m3_encode_array(vals))
+
+
+def test_bulk_encoder_refuses_ranges_past_the_last_pattern(oracle_lib):
+    with pytest.raises(ValueError):
+        oracle_lib.e4m3_encode_bits(0xFFFFFFF0, 17)

@@ -41,6 +41,7 @@ MUTANTS = [
      "return (uint8_t)(r / ldexp(1.0, -8));"),
     ("encode: values that round above 448 give NaN", "if (a >= ORA_E4M3_MAX)\n        return sign | 0x7E;",
      "if (a >= 464.0)\n        return sign | 0x7F;\n    if (a >= ORA_E4M3_MAX)\n        return sign | 0x7E;"),
+    ("bulk encoder: off by one pattern", "cv.u = first + (uint32_t)i;", "cv.u = first + (uint32_t)i + 1u;"),
     # scale and codes
     ("scale: no amax floor", "float a = amax > ORA_AMAX_FLOOR ? amax : ORA_AMAX_FLOOR;", "float a = amax;"),
     ("scale: divides by 480", "return (float)((double)a / ORA_E4M3_MAX);", "return (float)((double)a / 480.0);"),
