@@ -8,7 +8,9 @@ code must agree except on NaN inputs, where the pages say nothing about the
 sign of NaN: there both sides must give a NaN code (0x7F or 0xFF) and the
 device's choice is reported.
 
-The sweep itself runs on the GPU (marked gpu). The CPU tests check the sweep's
+The sweep itself runs on the GPU (marked gpu; this file sorts after the other
+GPU test files, so a stop at a first failure leaves them run). The CPU tests
+check the sweep's
 own logic, with the oracle standing in for the device: it finds no mismatch
 there, it finds planted ones, and it tolerates a NaN of the other sign.
 """
