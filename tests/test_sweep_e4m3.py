@@ -10,9 +10,9 @@ device's choice is reported.
 
 The sweep itself runs on the GPU (marked gpu; this file sorts after the other
 GPU test files, so a stop at a first failure leaves them run). The CPU tests
-check the sweep's
-own logic, with the oracle standing in for the device: it finds no mismatch
-there, it finds planted ones, and it tolerates a NaN of the other sign.
+check the sweep's own logic, with the oracle standing in for the device: it
+finds no mismatch there, it finds planted ones, and it tolerates a NaN of the
+other sign.
 """
 import os
 from concurrent.futures import ThreadPoolExecutor
