@@ -74,6 +74,12 @@ def _load():
         lib.ora_gemm_tensor_rows.restype = None
         lib.ora_gemm_tensor_points.argtypes = [P, F, P, F, I, P, P, I, P, P]
         lib.ora_gemm_tensor_points.restype = None
+        lib.ora_kv_store.argtypes = [P, I, I, P, I, F, P]
+        lib.ora_kv_store.restype = None
+        lib.ora_kv_load.argtypes = [P, I, I, P, I, F, P]
+        lib.ora_kv_load.restype = None
+        lib.ora_bf16_from_f32.argtypes = [P, I, P]
+        lib.ora_bf16_from_f32.restype = None
         _lib = lib
         return lib
 
@@ -169,6 +175,15 @@ def quant_weight_block(w_bf16: np.ndarray, block_n: int = 128, block_k: int = 12
     return quant_blocks(w_bf16, block_n, block_k, "rows_major")
 
 
+def quant_rowwise(x_bf16: np.ndarray):
+    """One scale per row (per-token activations, per-channel weights): the
+    block quantizer with blocks of 1 x cols. Returns (codes [rows, cols],
+    scales float32 [rows])."""
+    x = _bits16(x_bf16)
+    q, s = quant_blocks(x, 1, max(x.shape[1], 1), "cols_major")
+    return q, s.reshape(-1)
+
+
 def quant_per_tensor(x_bf16: np.ndarray, scale: float | None = None):
     """Per-tensor quantization; dynamic (scale from amax) when scale is None."""
     x = _bits16(x_bf16)
@@ -238,6 +253,25 @@ def gemm_grouped_points(qa, sa, qw, sw, offsets, ms, ns, gk=128, bn=128, bk=128)
     return y, ab
 
 
+def gemm_rowwise(qa, sa, qw, sw, rows=None):
+    """Per-token activation scales sa [M] and per-channel weight scales sw [N]:
+    the block-scaled GEMM with one activation group of all K per row and
+    weight blocks of 1 x K. Returns (Y [m1-m0, N], |a||b| sums)."""
+    M, K = np.shape(qa)
+    N = np.shape(qw)[0]
+    sa = np.asarray(sa, dtype=np.float32).reshape(1, M)
+    sw = np.asarray(sw, dtype=np.float32).reshape(N, 1)
+    return gemm_block(qa, sa, qw, sw, gk=K, bn=1, bk=K, rows=rows)
+
+
+def gemm_rowwise_points(qa, sa, qw, sw, ms, ns):
+    M, K = np.shape(qa)
+    N = np.shape(qw)[0]
+    sa = np.asarray(sa, dtype=np.float32).reshape(1, M)
+    sw = np.asarray(sw, dtype=np.float32).reshape(N, 1)
+    return gemm_block_points(qa, sa, qw, sw, ms, ns, gk=K, bn=1, bk=K)
+
+
 def gemm_tensor(qa, sa, qw, sw, rows=None):
     qa = np.ascontiguousarray(qa, dtype=np.uint8)
     qw = np.ascontiguousarray(qw, dtype=np.uint8)
@@ -269,3 +303,38 @@ def gemm_tensor_points(qa, sa, qw, sw, ms, ns):
 def tolerance(y_ref: np.ndarray, absdot: np.ndarray) -> np.ndarray:
     """Allowed |gpu - oracle|: 2e-3 * sum_k |a b| + 1e-2 * |oracle|."""
     return 2e-3 * absdot + 1e-2 * np.abs(y_ref)
+
+
+# -------------------------------------------------------------- KV cache ---
+
+def kv_store(x_bf16: np.ndarray, slots: np.ndarray, cache: np.ndarray, scale: float) -> np.ndarray:
+    """Store rows of x [T, E] (BF16 bits) into cache [S, E] (uint8, updated in
+    place and returned) at slots [T]; negative or out-of-range slots skipped."""
+    x = _bits16(x_bf16)
+    slots = np.ascontiguousarray(slots, dtype=np.int64)
+    assert cache.dtype == np.uint8 and cache.flags["C_CONTIGUOUS"] and cache.shape[1] == x.shape[1]
+    if x.shape[0]:
+        _load().ora_kv_store(_ptr(x), x.shape[0], x.shape[1], _ptr(slots), cache.shape[0], float(np.float32(scale)),
+                             _ptr(cache))
+    return cache
+
+
+def kv_load(cache: np.ndarray, slots: np.ndarray, out_bf16: np.ndarray, scale: float) -> np.ndarray:
+    """Rows of out [T, E] (BF16 bit patterns, uint16, updated in place and
+    returned) = cache rows slots[t] dequantized; skipped rows untouched."""
+    cache = np.ascontiguousarray(cache, dtype=np.uint8)
+    slots = np.ascontiguousarray(slots, dtype=np.int64)
+    assert out_bf16.dtype == np.uint16 and out_bf16.flags["C_CONTIGUOUS"] and out_bf16.shape[1] == cache.shape[1]
+    if out_bf16.shape[0]:
+        _load().ora_kv_load(_ptr(cache), out_bf16.shape[0], out_bf16.shape[1], _ptr(slots), cache.shape[0],
+                            float(np.float32(scale)), _ptr(out_bf16))
+    return out_bf16
+
+
+def bf16_from_f32(x: np.ndarray) -> np.ndarray:
+    """BF16 bit patterns of FP32 values (round to nearest even)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint16)
+    if x.size:
+        _load().ora_bf16_from_f32(_ptr(x), x.size, _ptr(out))
+    return out

@@ -326,3 +326,78 @@ void ora_gemm_tensor_points(const uint8_t *qa, float sa, const uint8_t *qw, floa
         ora_gemm_tensor_rows(qa + ms[i] * K, sa, qw + ns[i] * K, sw, 0, 1, 1, K,
                              &y[i], absdot ? &absdot[i] : NULL);
 }
+
+/* ------------------------------------------------------------ KV cache --- */
+
+/* BF16 bit pattern of an FP32 value: the nearest BF16 value (8 significant
+ * bits, the FP32 exponent range), ties to the even pattern; overflow rounds
+ * to infinity as in any IEEE binary format; NaN stays NaN (quiet, sign kept). */
+static uint16_t float_to_bf16_bits(float f)
+{
+    union { uint32_t u; float f; } cv;
+    double a, quantum, r;
+    int e2, exponent;
+    uint16_t sign;
+    cv.f = f;
+    sign = (uint16_t)((cv.u >> 16) & 0x8000u);
+    if (isnan(f))
+        return (uint16_t)(sign | 0x7FC0u);
+    a = fabs((double)f);
+    if (isinf(f) || a == 0.0) {
+        cv.f = f;
+        return (uint16_t)(cv.u >> 16);  /* +-Inf and +-0 are BF16 values */
+    }
+    /* binade 2^exponent <= a < 2^(exponent+1); below 2^-126 the spacing is
+     * that of the subnormals, 2^-133. 8 significant bits: quantum 2^(exponent-7). */
+    frexp(a, &e2);
+    exponent = e2 - 1;
+    if (exponent < -126)
+        exponent = -126;
+    quantum = ldexp(1.0, exponent - 7);
+    r = nearbyint(a / quantum) * quantum;  /* a / quantum is exact */
+    cv.f = (float)r;                       /* r is a BF16 value, or 2^128 -> Inf */
+    return (uint16_t)(sign | (uint16_t)((cv.u >> 16) & 0x7FFFu));
+}
+
+/*
+ * FP8 KV cache store ("[vLLM] FP8", section "KV 캐시 양자화": keys and values
+ * kept in FP8 with one scale per tensor). Row t of x [tokens][elems] goes to
+ * cache row slots[t] as e4m3(fl32(x / scale)); negative slots are padding and
+ * slots >= num_slots are skipped.
+ */
+void ora_kv_store(const uint16_t *x, int64_t tokens, int64_t elems, const int64_t *slots,
+                  int64_t num_slots, float scale, uint8_t *cache)
+{
+    int64_t t, e;
+    for (t = 0; t < tokens; t++) {
+        if (slots[t] < 0 || slots[t] >= num_slots)
+            continue;
+        for (e = 0; e < elems; e++)
+            cache[slots[t] * elems + e] = quant_value(bf16_bits_to_float(x[t * elems + e]), scale);
+    }
+}
+
+/* FP8 KV cache load: row t of out [tokens][elems] (BF16 bit patterns) is
+ * cache row slots[t] dequantized, bf16(fl32(dec(q) * scale)); the product of
+ * a code (4 significant bits) and an FP32 scale is exact in FP64, so the cast
+ * to float is the correctly rounded FP32 product. Skipped rows are untouched. */
+void ora_kv_load(const uint8_t *cache, int64_t tokens, int64_t elems, const int64_t *slots,
+                 int64_t num_slots, float scale, uint16_t *out)
+{
+    int64_t t, e;
+    for (t = 0; t < tokens; t++) {
+        if (slots[t] < 0 || slots[t] >= num_slots)
+            continue;
+        for (e = 0; e < elems; e++)
+            out[t * elems + e] = float_to_bf16_bits((float)(ora_e4m3_decode(cache[slots[t] * elems + e]) *
+                                                            (double)scale));
+    }
+}
+
+/* The BF16 rounding above, exposed for its pin against an independent cast. */
+void ora_bf16_from_f32(const float *x, int64_t n, uint16_t *out)
+{
+    int64_t i;
+    for (i = 0; i < n; i++)
+        out[i] = float_to_bf16_bits(x[i]);
+}
