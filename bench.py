@@ -521,6 +521,123 @@ def run_quant_section(torch, ops, dev, steps, warmup, peaks):
     return out
 
 
+def run_rowwise_section(torch, ops, dev, steps, warmup, peaks):
+    """Per-token activation x per-channel weight scales: decode shapes (M = 16,
+    the four projections, 8 layers of distinct weights back to back, GB/s)
+    and prefill shapes (M = 8192, each GEMM alone after an L2 flush, TFLOP/s)."""
+    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+    out = {"decode": {}, "prefill": {}}
+    weights = []
+    for layer in range(LAYERS):
+        per = []
+        for (N, K) in SHAPES:
+            w = synth.device_normal_bf16(N, K, 0, f"bench/rw/W/{layer}/{N}x{K}", sigma=0.02, device=dev)
+            per.append(ops.quant_rowwise(w))
+            del w
+        weights.append(per)
+    M = 16
+    acts = {}
+    for (N, K) in SHAPES:
+        cols = synth.pick(0, f"bench/X/outliers/{K}", K, int(round(0.001 * K)))
+        x = synth.device_normal_bf16(M, K, 0, f"bench/rw/X/{M}x{K}", outlier_cols=cols, outlier_scale=50.0,
+                                     device=dev)
+        qa, sa = ops.quant_rowwise(x)
+        acts[(N, K)] = (qa, sa, [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _ in range(LAYERS)])
+    reps = max(5, steps)
+    total_bytes, total_us = 0.0, 0.0
+    for i, (N, K) in enumerate(SHAPES):
+        qa, sa, ys = acts[(N, K)]
+
+        def g(marks, i=i, qa=qa, sa=sa, ys=ys):
+            for layer in range(LAYERS):
+                qw, sw = weights[layer][i]
+                ops.fp8_rowwise_gemm(qa, sa, qw, sw, ys[layer])
+        t = Timed(torch, g)
+        ms, _ = time_steps(torch, t.replay, reps, warmup)
+        us = ms * 1e3 / (reps * LAYERS)
+        nbytes = N * K + 4 * N + M * K + 4 * M + 2 * M * N
+        total_bytes += nbytes
+        total_us += us
+        out["decode"][f"M{M}_N{N}_K{K}"] = {"us": us, "GBps": nbytes / (us * 1e-6) / 1e9}
+    ach = total_bytes / (total_us * 1e-6) / 1e9
+    out["decode"]["roofline"] = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                 "frac": ach / peaks["hbm_gbs"], "peak_source": f"hbm_gbs of {peaks['source']}",
+                                 "timing": "events around a graph of 8 back-to-back GEMMs per shape"}
+    del weights, acts
+    wq = []
+    for (N, K) in SHAPES:
+        w = synth.device_normal_bf16(N, K, 0, f"bench/rw/Wp/{N}x{K}", sigma=0.02, device=dev)
+        wq.append(ops.quant_rowwise(w))
+        del w
+    calls = []
+    for i, (N, K) in enumerate(SHAPES):
+        Mp = 8192
+        x = synth.device_normal_bf16(Mp, K, 0, f"bench/rw/Xp/{K}", device=dev)
+        qa, sa = ops.quant_rowwise(x)
+        del x
+        calls.append((Mp, N, K, qa, sa, wq[i], torch.empty((Mp, N), dtype=torch.bfloat16, device=dev)))
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step(marks):
+        for j, (Mp, N, K, qa, sa, (qw, sw), y) in enumerate(calls):
+            flush.zero_()
+            if marks:
+                marks[j][0].record()
+            ops.fp8_rowwise_gemm(qa, sa, qw, sw, y)
+            if marks:
+                marks[j][1].record()
+    timed = Timed(torch, step, n_marks=len(calls))
+    time_steps(torch, timed.replay, steps, warmup)
+    if timed.ext:
+        kms = timed.mark_ms()
+        fl_total, ms_total = 0.0, 0.0
+        for j, (Mp, N, K, *_r) in enumerate(calls):
+            fl = 2.0 * Mp * N * K
+            fl_total += fl
+            ms_total += kms[j]
+            out["prefill"][f"M{Mp}_N{N}_K{K}"] = {"us": kms[j] * 1e3, "TFLOPS": fl / (kms[j] * 1e-3) / 1e12}
+        ach = fl_total / (ms_total * 1e-3) / 1e12
+        out["prefill"]["roofline"] = {"bound": "tensor", "achieved": ach, "peak": fp8_peak, "unit": "TFLOP/s",
+                                      "frac": ach / fp8_peak,
+                                      "peak_source": f"bf16_tflops of {peaks['source']} x {FP8_OVER_BF16}",
+                                      "timing": "each GEMM alone after a 256 MB L2 flush"}
+    del calls, wq, flush
+    return out
+
+
+def run_kv_section(torch, ops, dev, steps, warmup, peaks):
+    """FP8 KV cache: store one prefill batch of 8192 tokens (8 KV heads x 128,
+    keys and values) into random slots of a 65536-slot cache, and gather-load
+    all 65536 slots back to BF16. HBM GB/s of algorithmic bytes."""
+    T, E, S = 8192, 1024, 65536
+    k = synth.device_normal_bf16(T, E, 0, "bench/kv/k", device=dev)
+    v = synth.device_normal_bf16(T, E, 0, "bench/kv/v", device=dev)
+    kc = torch.zeros((S, E), dtype=torch.uint8, device=dev)
+    vc = torch.zeros((S, E), dtype=torch.uint8, device=dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(5)
+    slots = torch.randperm(S, generator=g, device=dev)[:T].contiguous()
+    all_slots = torch.randperm(S, generator=g, device=dev).contiguous()
+    ks = torch.tensor([0.02], dtype=torch.float32, device=dev)
+    vs = torch.tensor([0.015], dtype=torch.float32, device=dev)
+    ko = torch.empty((S, E), dtype=torch.bfloat16, device=dev)
+    vo = torch.empty((S, E), dtype=torch.bfloat16, device=dev)
+    out = {}
+    jobs = [("store 8192 tokens", lambda: ops.fp8_kv_cache_store(k, v, kc, vc, slots, ks, vs),
+             2 * T * E * 3 + 8 * T),
+            ("load 65536 slots", lambda: ops.fp8_kv_cache_load(kc, vc, ko, vo, all_slots, ks, vs),
+             2 * S * E * 3 + 8 * S)]
+    for name, fn, nbytes in jobs:
+        timed = Timed(torch, lambda marks, fn=fn: fn())
+        ms, _ = time_steps(torch, timed.replay, steps, warmup)
+        t = ms / steps * 1e-3
+        out[name] = {"us": t * 1e6, "GBps": nbytes / t / 1e9, "frac_hbm": nbytes / t / 1e9 / peaks["hbm_gbs"]}
+    out["note"] = ("E = 8 KV heads x 128; store reads BF16 K and V and writes E4M3 codes (3 B per element each), "
+                   "load reads codes and writes BF16; inputs of 33.6 / 134 MB vs the 129 MB L2")
+    del k, v, kc, vc, ko, vo
+    return out
+
+
 # --------------------------------------------------------------- CPU legs --
 
 def oracle_decode_sample(budget_s: float):
@@ -691,7 +808,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--sections", default="prefill,tensor,moe,quant")
+    ap.add_argument("--sections", default="prefill,tensor,moe,quant,rowwise,kv")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--case", default=None, help="profile one kernel: KIND:M:N:K")
     ap.add_argument("--launches", type=int, default=3)
@@ -731,7 +848,8 @@ def main():
         wanted = [s for s in args.sections.split(",") if s]
         sec_steps = max(5, min(args.steps, 30))
         for name, fn in [("prefill", run_prefill_section), ("tensor", run_tensor_section),
-                         ("moe", run_moe_section), ("quant", run_quant_section)]:
+                         ("moe", run_moe_section), ("quant", run_quant_section),
+                         ("rowwise", run_rowwise_section), ("kv", run_kv_section)]:
             if name in wanted:
                 torch.cuda.empty_cache()
                 sections[name] = fn(torch, ops, dev, sec_steps, 3, peaks)

@@ -27,6 +27,10 @@ SIGNATURES = {
     "fp8_block_gemm": ([P, P, P, P, P, I64, I64, I64, I32, I32, I32, I32, P, P], I32),
     "fp8_tensor_gemm": ([P, P, P, P, P, I64, I64, I64, P], I32),
     "fp8_block_linear": ([P, P, P, P, P, P, I64, I64, I64, P], I32),
+    "fp8_quant_rowwise": ([P, P, P, I64, I64, P], I32),
+    "fp8_rowwise_gemm": ([P, P, P, P, P, I64, I64, I64, P], I32),
+    "fp8_kv_cache_store": ([P, P, P, P, P, P, P, I64, I64, I64, P], I32),
+    "fp8_kv_cache_load": ([P, P, P, P, P, P, P, I64, I64, I64, P], I32),
     "fp8_status_string": ([I32], ctypes.c_char_p),
     "fp8_device_error": ([P, ctypes.POINTER(I32), ctypes.POINTER(I32)], I32),
     "fp8_selftest_bounded_wait": ([P], I32),

@@ -16,7 +16,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libfp8w8a8.so")
-SOURCES = ["api.cu", "quant.cu", "gemm_prefill.cu", "gemm_decode.cu", "selftest.cu"]
+SOURCES = ["api.cu", "quant.cu", "gemm_prefill.cu", "gemm_decode.cu", "kv_cache.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -93,7 +93,7 @@ int fp8_quant_act_group(const void *x_bf16, void *q_e4m3, float *scales, int64_t
                         void *stream) {
     if (M < 0 || K < 0) return FP8_ERR_SHAPE;
     if (group_k != FP8_GROUP) return FP8_ERR_UNSUPPORTED;
-    if (K == 0 || K % FP8_GROUP != 0 || M > INT_MAX || K > INT_MAX) return FP8_ERR_SHAPE;
+    if (K == 0 || K % FP8_GROUP != 0 || M > INT_MAX || K > FP8_ACT_GROUP_MAX_K) return FP8_ERR_SHAPE;
     if (M == 0) return FP8_OK;
     if (!x_bf16 || !q_e4m3 || !scales) return FP8_ERR_NULL;
     if (misaligned(x_bf16, 16) || misaligned(q_e4m3, 16) || misaligned(scales, 4)) return FP8_ERR_ALIGN;
@@ -107,7 +107,7 @@ int fp8_quant_weight_block(const void *w_bf16, void *q_e4m3, float *scales, int6
                            int block_k, void *stream) {
     if (N < 0 || K < 0) return FP8_ERR_SHAPE;
     if (block_n != FP8_GROUP || block_k != FP8_GROUP) return FP8_ERR_UNSUPPORTED;
-    if (K == 0 || K % FP8_GROUP != 0 || N > INT_MAX || K > INT_MAX) return FP8_ERR_SHAPE;
+    if (K == 0 || K % FP8_GROUP != 0 || N > FP8_WEIGHT_BLOCK_MAX_N || K > INT_MAX) return FP8_ERR_SHAPE;
     if (N == 0) return FP8_OK;
     if (!w_bf16 || !q_e4m3 || !scales) return FP8_ERR_NULL;
     if (misaligned(w_bf16, 16) || misaligned(q_e4m3, 16) || misaligned(scales, 4)) return FP8_ERR_ALIGN;
@@ -151,9 +151,9 @@ int fp8_block_gemm(const void *qa, const float *sa, const void *qw, const float 
     if (int st = fp8k::current_device(&dev)) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (group_offsets == nullptr && M <= 16)
-        return fp8k::to_status(fp8k::launch_gemm_decode(qa, sa, qw, sw, y_bf16, M, N, K, false, *dev, s));
+        return fp8k::to_status(fp8k::launch_gemm_decode(qa, sa, qw, sw, y_bf16, M, N, K, fp8k::kScaleBlock, *dev, s));
     return fp8k::to_status(fp8k::launch_gemm_prefill(qa, sa, qw, sw, y_bf16, M, N, K, num_groups, group_offsets,
-                                                     false, *dev, s));
+                                                     fp8k::kScaleBlock, *dev, s));
 }
 
 int fp8_tensor_gemm(const void *qa, const float *sa, const void *qw, const float *sw, void *y_bf16, int64_t M,
@@ -169,9 +169,9 @@ int fp8_tensor_gemm(const void *qa, const float *sa, const void *qw, const float
     const fp8k::DeviceInfo *dev = nullptr;
     if (int st = fp8k::current_device(&dev)) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (M <= 16) return fp8k::to_status(fp8k::launch_gemm_decode(qa, sa, qw, sw, y_bf16, M, N, K, true, *dev, s));
+    if (M <= 16) return fp8k::to_status(fp8k::launch_gemm_decode(qa, sa, qw, sw, y_bf16, M, N, K, fp8k::kScaleTensor, *dev, s));
     return fp8k::to_status(
-        fp8k::launch_gemm_prefill(qa, sa, qw, sw, y_bf16, M, N, K, 1, nullptr, true, *dev, s));
+        fp8k::launch_gemm_prefill(qa, sa, qw, sw, y_bf16, M, N, K, 1, nullptr, fp8k::kScaleTensor, *dev, s));
 }
 
 int fp8_block_linear(const void *x_bf16, void *qa, float *sa, const void *qw, const float *sw, void *y_bf16,
@@ -189,8 +189,80 @@ int fp8_block_linear(const void *x_bf16, void *qa, float *sa, const void *qw, co
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = fp8k::launch_quant_act_group(x_bf16, qa, sa, M, K, *dev, s);
     if (e != cudaSuccess) return FP8_ERR_CUDA;
-    if (M <= 16) return fp8k::to_status(fp8k::launch_gemm_decode(qa, sa, qw, sw, y_bf16, M, N, K, false, *dev, s));
-    return fp8k::to_status(fp8k::launch_gemm_prefill(qa, sa, qw, sw, y_bf16, M, N, K, 1, nullptr, false, *dev, s));
+    if (M <= 16) return fp8k::to_status(fp8k::launch_gemm_decode(qa, sa, qw, sw, y_bf16, M, N, K, fp8k::kScaleBlock, *dev, s));
+    return fp8k::to_status(fp8k::launch_gemm_prefill(qa, sa, qw, sw, y_bf16, M, N, K, 1, nullptr, fp8k::kScaleBlock, *dev, s));
+}
+
+int fp8_quant_rowwise(const void *x_bf16, void *q_e4m3, float *scales, int64_t rows, int64_t cols, void *stream) {
+    if (rows < 0 || cols < 0) return FP8_ERR_SHAPE;
+    if (cols == 0 || cols % 16 != 0 || rows > INT_MAX || cols > INT_MAX) return FP8_ERR_SHAPE;
+    if (rows == 0) return FP8_OK;
+    if (!x_bf16 || !q_e4m3 || !scales) return FP8_ERR_NULL;
+    if (misaligned(x_bf16, 16) || misaligned(q_e4m3, 16) || misaligned(scales, 4)) return FP8_ERR_ALIGN;
+    const fp8k::DeviceInfo *dev = nullptr;
+    if (int st = fp8k::current_device(&dev)) return st;
+    return fp8k::to_status(
+        fp8k::launch_quant_rows(x_bf16, q_e4m3, scales, rows, cols, *dev, static_cast<cudaStream_t>(stream)));
+}
+
+int fp8_rowwise_gemm(const void *qa, const float *sa, const void *qw, const float *sw, void *y_bf16, int64_t M,
+                     int64_t N, int64_t K, void *stream) {
+    if (M < 0 || N < 0 || K < 0) return FP8_ERR_SHAPE;
+    if (K == 0 || K % 16 != 0 || N == 0 || N % 16 != 0) return FP8_ERR_SHAPE;
+    if (M > INT_MAX || N > INT_MAX || K > INT_MAX) return FP8_ERR_SHAPE;
+    if (M == 0) return FP8_OK;
+    if (!qa || !sa || !qw || !sw || !y_bf16) return FP8_ERR_NULL;
+    if (misaligned(qa, 16) || misaligned(qw, 16) || misaligned(y_bf16, 16) || misaligned(sa, 4) ||
+        misaligned(sw, 16))
+        return FP8_ERR_ALIGN;
+    const fp8k::DeviceInfo *dev = nullptr;
+    if (int st = fp8k::current_device(&dev)) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (M <= 16)
+        return fp8k::to_status(fp8k::launch_gemm_decode(qa, sa, qw, sw, y_bf16, M, N, K, fp8k::kScaleRowCol, *dev, s));
+    return fp8k::to_status(
+        fp8k::launch_gemm_prefill(qa, sa, qw, sw, y_bf16, M, N, K, 1, nullptr, fp8k::kScaleRowCol, *dev, s));
+}
+
+static int kv_check(const void *a, const void *b, const void *c, const void *d, const int64_t *slots,
+                    const float *ks, const float *vs, int64_t tokens, int64_t elems, int64_t num_slots) {
+    if (tokens < 0 || elems < 0 || num_slots < 0) return FP8_ERR_SHAPE;
+    if (elems == 0 || elems % 16 != 0 || tokens > INT_MAX || elems > INT_MAX) return FP8_ERR_SHAPE;
+    if (num_slots > INT64_MAX / elems) return FP8_ERR_SHAPE;
+    if (tokens == 0) return FP8_OK;
+    if (!a || !b || !c || !d || !slots || !ks || !vs) return FP8_ERR_NULL;
+    if (misaligned(a, 16) || misaligned(b, 16) || misaligned(c, 16) || misaligned(d, 16) || misaligned(slots, 8) ||
+        misaligned(ks, 4) || misaligned(vs, 4))
+        return FP8_ERR_ALIGN;
+    return FP8_OK;
+}
+
+int fp8_kv_cache_store(const void *key_bf16, const void *value_bf16, void *key_cache, void *value_cache,
+                       const int64_t *slot_mapping, const float *k_scale, const float *v_scale, int64_t num_tokens,
+                       int64_t token_elems, int64_t num_slots, void *stream) {
+    if (int st = kv_check(key_bf16, value_bf16, key_cache, value_cache, slot_mapping, k_scale, v_scale, num_tokens,
+                          token_elems, num_slots))
+        return st;
+    if (num_tokens == 0) return FP8_OK;
+    const fp8k::DeviceInfo *dev = nullptr;
+    if (int st = fp8k::current_device(&dev)) return st;
+    return fp8k::to_status(fp8k::launch_kv_store(key_bf16, value_bf16, key_cache, value_cache, slot_mapping, k_scale,
+                                                 v_scale, num_tokens, token_elems, num_slots, *dev,
+                                                 static_cast<cudaStream_t>(stream)));
+}
+
+int fp8_kv_cache_load(const void *key_cache, const void *value_cache, void *key_bf16, void *value_bf16,
+                      const int64_t *slot_mapping, const float *k_scale, const float *v_scale, int64_t num_tokens,
+                      int64_t token_elems, int64_t num_slots, void *stream) {
+    if (int st = kv_check(key_cache, value_cache, key_bf16, value_bf16, slot_mapping, k_scale, v_scale, num_tokens,
+                          token_elems, num_slots))
+        return st;
+    if (num_tokens == 0) return FP8_OK;
+    const fp8k::DeviceInfo *dev = nullptr;
+    if (int st = fp8k::current_device(&dev)) return st;
+    return fp8k::to_status(fp8k::launch_kv_load(key_cache, value_cache, key_bf16, value_bf16, slot_mapping, k_scale,
+                                                v_scale, num_tokens, token_elems, num_slots, *dev,
+                                                static_cast<cudaStream_t>(stream)));
 }
 
 const char *fp8_status_string(int status) {

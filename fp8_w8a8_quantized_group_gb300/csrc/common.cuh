@@ -59,6 +59,48 @@ __device__ __forceinline__ uint2 quant8(const uint4 &v, float s) {
     return r;
 }
 
+// The E4M3 code pair of two FP32 values (low byte = a): the hardware's
+// round-to-nearest-even, saturating conversion.
+__device__ __forceinline__ uint32_t e4m3_pair(float a, float b) {
+    return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
+}
+
+// Same codes as quant8(v, s) - those of the correctly rounded quotients
+// RN(x/s) - for kernels bound by instruction issue, with r = RN(1/s)
+// computed once by the caller. q = RN(x*r) carries two roundings, so it lies
+// within 1.5 * 2^-23 |q| of RN(x/s), while RN(q * (1 -+ 2^-21)) lie more than
+// 3.5 * 2^-23 |q| away on either side: RN(x/s) lies between them. Rounding to
+// nearest even and saturating is monotonic, so when both bounds convert to
+// the codes of q, so does RN(x/s). Otherwise (near a rounding boundary of the
+// conversion), and whenever r overflows (s zero or subnormal, where x*r
+// could be 0 * Inf), the chunk takes correctly rounded divisions.
+__device__ __forceinline__ uint2 quant8_recip(const uint4 &v, float s, float r) {
+    const float x[8] = {bf16lo(v.x), bf16hi(v.x), bf16lo(v.y), bf16hi(v.y),
+                        bf16lo(v.z), bf16hi(v.z), bf16lo(v.w), bf16hi(v.w)};
+    constexpr float kDown = 1.0f - 0x1p-21f, kUp = 1.0f + 0x1p-21f;  // both exact in FP32
+    float q[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] = __fmul_rn(x[i], r);
+    uint2 out, lo, hi;
+    out.x = e4m3_pair(q[0], q[1]) | (e4m3_pair(q[2], q[3]) << 16);
+    out.y = e4m3_pair(q[4], q[5]) | (e4m3_pair(q[6], q[7]) << 16);
+    lo.x = e4m3_pair(__fmul_rn(q[0], kDown), __fmul_rn(q[1], kDown)) |
+           (e4m3_pair(__fmul_rn(q[2], kDown), __fmul_rn(q[3], kDown)) << 16);
+    lo.y = e4m3_pair(__fmul_rn(q[4], kDown), __fmul_rn(q[5], kDown)) |
+           (e4m3_pair(__fmul_rn(q[6], kDown), __fmul_rn(q[7], kDown)) << 16);
+    hi.x = e4m3_pair(__fmul_rn(q[0], kUp), __fmul_rn(q[1], kUp)) |
+           (e4m3_pair(__fmul_rn(q[2], kUp), __fmul_rn(q[3], kUp)) << 16);
+    hi.y = e4m3_pair(__fmul_rn(q[4], kUp), __fmul_rn(q[5], kUp)) |
+           (e4m3_pair(__fmul_rn(q[6], kUp), __fmul_rn(q[7], kUp)) << 16);
+    if ((lo.x != out.x) | (lo.y != out.y) | (hi.x != out.x) | (hi.y != out.y) | (fabsf(r) == INFINITY)) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) q[i] = __fdiv_rn(x[i], s);
+        out.x = e4m3_pair(q[0], q[1]) | (e4m3_pair(q[2], q[3]) << 16);
+        out.y = e4m3_pair(q[4], q[5]) | (e4m3_pair(q[6], q[7]) << 16);
+    }
+    return out;
+}
+
 __device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
     uint4 r;
     asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -69,6 +111,7 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
 // ----------------------------------------------------------------- errors --
 
 // Error word layout: err[0] = first status recorded (0 = none), err[1] = site.
+constexpr unsigned kErrArg = 5;      // FP8_ERR_ARG: an argument checked on the device
 constexpr unsigned kErrTimeout = 8;  // FP8_ERR_TIMEOUT
 // A bounded wait gives up after this long (nanoseconds of %globaltimer).
 constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;

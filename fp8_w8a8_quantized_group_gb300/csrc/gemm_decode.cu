@@ -30,7 +30,9 @@
 //    write is made, after griddepcontrol.wait.
 //
 // Block mode applies Sw[n/128][kb] * Sa[kb][m] per K block; per-tensor mode
-// accumulates all of the CTA's K range in TMEM and applies sa * sw once.
+// accumulates all of the CTA's K range in TMEM and applies sa * sw once;
+// row/column mode does the same with sa[m] * sw[n] (per-token activation and
+// per-channel weight scales).
 #include <mutex>
 
 #include "common.cuh"
@@ -57,11 +59,12 @@ constexpr int kSmemBytes =
 enum : unsigned { kSiteProdEmpty = 201, kSiteMmaTmem = 202, kSiteMmaFull = 203, kSiteEpiFull = 204,
                   kSiteDrain = 205, kSiteReduce = 206 };
 
-template <bool PER_TENSOR>
+template <int MODE>
 __global__ void __launch_bounds__(kThreads, 2)
     gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                        const float *__restrict__ sa, const float *__restrict__ sw,
                        __nv_bfloat16 *__restrict__ y, int M, int N, int K, int splits, unsigned *err) {
+    constexpr bool WHOLE_K = MODE != kScaleBlock;  // all of the CTA's K in one TMEM accumulator
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sW = smem;
@@ -157,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             bool any = false;
             for (int kb = kb0; kb < kb1; ++kb) {
                 const bool first = kb == kb0, last = kb == kb1 - 1;
-                if (!PER_TENSOR || first) {
+                if (!WHOLE_K || first) {
                     if (!mbar_wait<true>(&tempty[buf], bphase ^ 1u, abort_flag, err, kSiteMmaTmem)) break;
                     tc_fence_after();
                 }
@@ -168,14 +171,14 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const uint32_t d = tmem_base + buf * kTok;
 #pragma unroll
                 for (int k = 0; k < BK / 32; ++k) {
-                    const uint32_t accum = (k > 0 || (PER_TENSOR && !first)) ? 1u : 0u;
+                    const uint32_t accum = (k > 0 || (WHOLE_K && !first)) ? 1u : 0u;
                     umma_e4m3(d, sdesc_k_sw128(w0 + k * 32), sdesc_k_sw128(x0 + k * 32), idesc, accum);
                 }
                 umma_commit(&empty[stage]);
                 any = true;
                 last_stage = stage;
                 last_phase = phase;
-                if (!PER_TENSOR || last) {
+                if (!WHOLE_K || last) {
                     umma_commit(&tfull[buf]);
                     if (++buf == 2) { buf = 0; bphase ^= 1u; }
                 }
@@ -195,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(ep * 32) << 16);
         uint32_t buf = 0, bphase = 0;
         grid_dep_wait();
-        if (!PER_TENSOR) {
+        if (!WHOLE_K) {
             // Scales of kScaleKb K blocks at a time go through this warp's own
             // shared-memory slice; the next chunk is loaded into registers while
             // the current one is used (one L2 round trip per chunk, not per block).
@@ -246,9 +249,17 @@ __global__ void __launch_bounds__(kThreads, 2)
                 float p[kTok];
                 tmem_ld16(lane_addr, p);
                 tc_fence_before();
-                const float sc = sa[0] * sw[0];
+                if (MODE == kScaleTensor) {
+                    const float sc = sa[0] * sw[0];
 #pragma unroll
-                for (int j = 0; j < kTok; ++j) acc[j] = p[j] * sc;
+                    for (int j = 0; j < kTok; ++j) acc[j] = p[j] * sc;
+                } else {  // per token (sa[j]) and per output channel (sw[n])
+                    const int n = n0 + r;
+                    const float swn = n < N ? __ldg(sw + n) : 0.0f;
+#pragma unroll
+                    for (int j = 0; j < kTok; ++j)
+                        if (j < M) acc[j] = p[j] * (__ldg(sa + j) * swn);
+                }
             }
         }
         if (splits == 1) {
@@ -343,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 }
 
-template <bool PER_TENSOR>
+template <int MODE>
 cudaError_t launch_variant(const void *qa, const float *sa, const void *qw, const float *sw, void *y, int64_t M,
                            int64_t N, int64_t K, const DeviceInfo &dev, cudaStream_t stream) {
     static std::once_flag attr_once[64];
@@ -351,7 +362,7 @@ cudaError_t launch_variant(const void *qa, const float *sa, const void *qw, cons
     int device = 0;
     cudaGetDevice(&device);
     std::call_once(attr_once[device & 63], [&] {
-        cudaError_t e = cudaFuncSetAttribute(gemm_decode_kernel<PER_TENSOR>,
+        cudaError_t e = cudaFuncSetAttribute(gemm_decode_kernel<MODE>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         attr_err[device & 63] = e;
     });
@@ -382,7 +393,7 @@ cudaError_t launch_variant(const void *qa, const float *sa, const void *qw, cons
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, gemm_decode_kernel<PER_TENSOR>, tmW, tmX, sa, sw,
+    return cudaLaunchKernelEx(&cfg, gemm_decode_kernel<MODE>, tmW, tmX, sa, sw,
                               static_cast<__nv_bfloat16 *>(y), static_cast<int>(M), static_cast<int>(N),
                               static_cast<int>(K), splits, dev.err);
 }
@@ -390,10 +401,11 @@ cudaError_t launch_variant(const void *qa, const float *sa, const void *qw, cons
 }  // namespace
 
 cudaError_t launch_gemm_decode(const void *qa, const float *sa, const void *qw, const float *sw, void *y,
-                               int64_t M, int64_t N, int64_t K, bool per_tensor, const DeviceInfo &dev,
+                               int64_t M, int64_t N, int64_t K, ScaleMode mode, const DeviceInfo &dev,
                                cudaStream_t stream) {
-    if (per_tensor) return launch_variant<true>(qa, sa, qw, sw, y, M, N, K, dev, stream);
-    return launch_variant<false>(qa, sa, qw, sw, y, M, N, K, dev, stream);
+    if (mode == kScaleTensor) return launch_variant<kScaleTensor>(qa, sa, qw, sw, y, M, N, K, dev, stream);
+    if (mode == kScaleRowCol) return launch_variant<kScaleRowCol>(qa, sa, qw, sw, y, M, N, K, dev, stream);
+    return launch_variant<kScaleBlock>(qa, sa, qw, sw, y, M, N, K, dev, stream);
 }
 
 }  // namespace fp8k

@@ -25,11 +25,12 @@
 //    scale promotion) and, after the last K block, writes its half-row as BF16;
 //  - warpgroup 0 gives registers to the epilogue warpgroups (setmaxnreg);
 //  - per-tensor mode: the MMAs accumulate all of K in TMEM; the epilogue
-//    applies the single scale product once per tile, streaming TMEM to Y.
+//    applies the single scale product once per tile, streaming TMEM to Y;
+//    row/column mode likewise, with sa[m] * sw[n] (per-token activation and
+//    per-channel weight scales).
 //
 // Every wait is bounded (common.cuh); on expiry the CTA records an error,
 // stops issuing, lets the copies and MMAs it issued finish and frees TMEM.
-#include <cstdlib>
 #include <mutex>
 
 #include "common.cuh"
@@ -49,9 +50,9 @@ constexpr int kTmemCols = 512;
 // compiled with); the launcher checks that before every launch. The 128 x 256
 // block-scaled epilogue holds 128 accumulators and two 16-column load buffers
 // per thread, so it takes the larger share.
-template <int BN, bool PER_TENSOR>
+template <int BN, bool WHOLE_K>
 struct RegSplit {
-    static constexpr bool kWide = BN == 256 && !PER_TENSOR;
+    static constexpr bool kWide = BN == 256 && !WHOLE_K;
     static constexpr int kLow = kWide ? 56 : 72;
     static constexpr int kHigh = kWide ? 224 : 216;
     static_assert(128 * kLow + 256 * kHigh <= 384 * 168, "register split exceeds the launch budget");
@@ -59,7 +60,7 @@ struct RegSplit {
 
 // Bounded-wait sites reported through the error word.
 enum : unsigned { kSiteProdEmpty = 101, kSiteMmaTmem = 102, kSiteMmaFull = 103, kSiteEpiFull = 104,
-                  kSiteDrain = 105 };
+                  kSiteDrain = 105, kSiteOffsets = 106 };
 
 template <int BN>
 struct Cfg {
@@ -118,6 +119,18 @@ __device__ __forceinline__ void tmem_ld_chunk<64>(uint32_t taddr, float (&p)[64]
 template <>
 __device__ __forceinline__ void tmem_ld_chunk<32>(uint32_t taddr, float (&p)[32]) { tmem_ld32(taddr, p); }
 
+// Eight outputs p[j] * (s * sw[j]): one row scale, eight column scales.
+__device__ __forceinline__ uint4 pack8_rowcol(const float *p, float s, const float *swp) {
+    const float4 a = __ldg(reinterpret_cast<const float4 *>(swp));
+    const float4 b = __ldg(reinterpret_cast<const float4 *>(swp + 4));
+    uint4 v;
+    v.x = pack_bf16x2(p[0] * (s * a.x), p[1] * (s * a.y));
+    v.y = pack_bf16x2(p[2] * (s * a.z), p[3] * (s * a.w));
+    v.z = pack_bf16x2(p[4] * (s * b.x), p[5] * (s * b.y));
+    v.w = pack_bf16x2(p[6] * (s * b.z), p[7] * (s * b.w));
+    return v;
+}
+
 __device__ __forceinline__ uint4 pack8_scaled(const float *p, float s) {
     uint4 v;
     v.x = pack_bf16x2(p[0] * s, p[1] * s);
@@ -127,14 +140,15 @@ __device__ __forceinline__ uint4 pack8_scaled(const float *p, float s) {
     return v;
 }
 
-template <int BN, bool PER_TENSOR>
+template <int BN, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const float *__restrict__ sa, const float *__restrict__ sw,
                         __nv_bfloat16 *__restrict__ y, int M, int N, int K, int groups,
                         const int32_t *__restrict__ offsets, int raster, unsigned *err) {
     using C = Cfg<BN>;
-    constexpr uint32_t kIssuers = PER_TENSOR ? 1u : 2u;  // MMA-issuing lanes
+    constexpr bool WHOLE_K = MODE != kScaleBlock;  // all of K in one TMEM accumulator per tile
+    constexpr uint32_t kIssuers = WHOLE_K ? 1u : 2u;  // MMA-issuing lanes
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sA = smem;
@@ -162,9 +176,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (offsets != nullptr) {
             // Expert e owns rows [lo, hi) clamped into [0, M]; its tiles follow
             // those of experts < e (expert-major, n fastest within an expert).
+            // Offsets that are not non-decreasing within [0, M] are a caller
+            // error, recorded (by CTA 0) as FP8_ERR_ARG; they are clamped so
+            // that no access leaves the buffers.
             int acc = 0;
+            bool bad = false;
             for (int e = 0; e < groups; ++e) {
                 int lo = offsets[e], hi = offsets[e + 1];
+                bad |= lo < 0 || hi < lo || hi > M;
                 lo = lo < 0 ? 0 : (lo > M ? M : lo);
                 hi = hi < lo ? lo : (hi > M ? M : hi);
                 t_lo[e] = lo;
@@ -173,6 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 acc += ((hi - lo + BM - 1) / BM) * num_n;
             }
             t_start[groups] = acc;
+            if (bad && blockIdx.x == 0) record_error(err, kErrArg, kSiteOffsets);
         }
     }
     if (warp == 0 && lane == 0) { tma_prefetch_desc(&tmA); tma_prefetch_desc(&tmB); }
@@ -189,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int total = offsets != nullptr ? t_start[groups] : sched.num_m * num_n;
 
     if (warp < 4) {
-        regs_shrink<RegSplit<BN, PER_TENSOR>::kLow>();
+        regs_shrink<RegSplit<BN, WHOLE_K>::kLow>();
         if (warp == 0 && lane == 0) {
             // ------------------------------------------------ TMA producer --
             uint32_t stage = 0, phase = 0;
@@ -237,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 for (int kb = 0; kb < Kg && ok; ++kb, ++gi) {
                     if (gi % kIssuers == own) {
-                        if (!PER_TENSOR || kb == 0) {
+                        if (!WHOLE_K || kb == 0) {
                             ok = mbar_wait<true>(&tempty[buf], bphase ^ 1u, abort_flag, err, kSiteMmaTmem);
                             if (!ok) break;
                         }
@@ -249,21 +269,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t d = tmem_base + buf * BN;
 #pragma unroll
                         for (int k = 0; k < BK / 32; ++k) {
-                            const uint32_t acc = (k > 0 || (PER_TENSOR && kb > 0)) ? 1u : 0u;
+                            const uint32_t acc = (k > 0 || (WHOLE_K && kb > 0)) ? 1u : 0u;
                             umma_e4m3(d, sdesc_k_sw128(a0 + k * 32), sdesc_k_sw128(b0 + k * 32), idesc, acc);
                         }
-                        if (PER_TENSOR) {
+                        if (WHOLE_K) {
                             umma_commit(&empty[stage]);
                             last_bar = &empty[stage];
                             last_parity = phase;
                         }
-                        if (!PER_TENSOR || kb == Kg - 1) {
+                        if (!WHOLE_K || kb == Kg - 1) {
                             umma_commit(&tfull[buf]);
                             last_bar = &tfull[buf];
                             last_parity = bphase;
                         }
                     }
-                    if (!PER_TENSOR || kb == Kg - 1) {
+                    if (!WHOLE_K || kb == Kg - 1) {
                         if (++buf == C::kBufs) { buf = 0; bphase ^= 1u; }
                     }
                     if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
@@ -281,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();  // lanes 1..31 wait for their lane 0
     } else {
-        regs_grow<RegSplit<BN, PER_TENSOR>::kHigh>();
+        regs_grow<RegSplit<BN, WHOLE_K>::kHigh>();
         // ------------------------------------------------------ epilogue --
         const int quarter = warp & 3;      // TMEM lane quarter this warp may access
         const int half = (warp - 4) >> 2;  // which half of the tile's columns
@@ -292,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t stage = 0;  // shared-memory stage of the current K block (block-scaled mode)
         const bool frees_stages = (warp == 4 && lane == 0);
         float tensor_scale = 0.0f;
-        if (PER_TENSOR) tensor_scale = sa[0] * sw[0];
+        if (MODE == kScaleTensor) tensor_scale = sa[0] * sw[0];
         bool ok = true;
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
             const Tile tl = sched.get(t);
@@ -300,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool row_in = m < M;
             const bool row_out = row_in && m < tl.row_end;
             __nv_bfloat16 *yrow = y + static_cast<int64_t>(m) * N + tl.n0 + c0;
-            if (!PER_TENSOR) {
+            if (!WHOLE_K) {
                 float acc[C::kCols];
 #pragma unroll
                 for (int j = 0; j < C::kCols; ++j) acc[j] = 0.0f;
@@ -370,11 +390,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mbar_arrive(&tempty[buf]);
                     }
                     if (row_out) {
+                        // Row/column mode: this row's token scale times each
+                        // column's channel scale (loaded per 8 columns).
+                        const float srow = MODE == kScaleRowCol ? __ldg(sa + m) : 0.0f;
 #pragma unroll
                         for (int q = 0; q < C::kChunk / 8; ++q) {
                             const int col = c * C::kChunk + q * 8;
-                            if (tl.n0 + c0 + col < N)
-                                *reinterpret_cast<uint4 *>(yrow + col) = pack8_scaled(p + q * 8, tensor_scale);
+                            if (tl.n0 + c0 + col < N) {
+                                if (MODE == kScaleRowCol)
+                                    *reinterpret_cast<uint4 *>(yrow + col) =
+                                        pack8_rowcol(p + q * 8, srow, sw + tl.n0 + c0 + col);
+                                else
+                                    *reinterpret_cast<uint4 *>(yrow + col) = pack8_scaled(p + q * 8, tensor_scale);
+                            }
                         }
                     }
                 }
@@ -391,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int BN, bool PER_TENSOR>
+template <int BN, int MODE>
 cudaError_t launch_variant(const void *qa, const float *sa, const void *qw, const float *sw, void *y, int64_t M,
                            int64_t N, int64_t K, int num_groups, const int32_t *offsets, const DeviceInfo &dev,
                            cudaStream_t stream) {
@@ -401,13 +429,13 @@ cudaError_t launch_variant(const void *qa, const float *sa, const void *qw, cons
     int device = 0;
     cudaGetDevice(&device);
     std::call_once(attr_once[device & 63], [&] {
-        cudaError_t e = cudaFuncSetAttribute(gemm_prefill_kernel<BN, PER_TENSOR>,
+        cudaError_t e = cudaFuncSetAttribute(gemm_prefill_kernel<BN, MODE>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
         // The register re-split inside the kernel needs the launch to hold at
         // least 128 * kLow + 256 * kHigh registers; refuse otherwise.
-        using S = RegSplit<BN, PER_TENSOR>;
+        using S = RegSplit<BN, MODE != kScaleBlock>;
         cudaFuncAttributes fa;
-        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, gemm_prefill_kernel<BN, PER_TENSOR>);
+        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, gemm_prefill_kernel<BN, MODE>);
         if (e == cudaSuccess && fa.numRegs * kThreads < 128 * S::kLow + 256 * S::kHigh)
             e = cudaErrorInvalidConfiguration;
         attr_err[device & 63] = e;
@@ -428,35 +456,28 @@ cudaError_t launch_variant(const void *qa, const float *sa, const void *qw, cons
     // Tiles sharing a row panel run together when the weight operand is the
     // smaller one (it stays in L2 while activations stream), else the reverse.
     const int raster = (N <= M) ? 0 : 1;
-    gemm_prefill_kernel<BN, PER_TENSOR><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(
+    gemm_prefill_kernel<BN, MODE><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(
         tmA, tmB, sa, sw, static_cast<__nv_bfloat16 *>(y), static_cast<int>(M), static_cast<int>(N),
         static_cast<int>(K), num_groups, offsets, raster, dev.err);
     return cudaGetLastError();
 }
 
-// Tile width: FP8_PREFILL_BN=128|256 overrides the default (256 when N is a
-// multiple of 256, else 128).
-int pick_bn(int64_t N) {
-    static const int forced = [] {
-        const char *v = std::getenv("FP8_PREFILL_BN");
-        return v ? std::atoi(v) : 0;
-    }();
-    if (forced == 128 || forced == 256) return forced;
-    return (N % 256 == 0) ? 256 : 128;
-}
+// Tile width: 256 when N is a multiple of 256, else 128.
+int pick_bn(int64_t N) { return (N % 256 == 0) ? 256 : 128; }
 
 }  // namespace
 
 cudaError_t launch_gemm_prefill(const void *qa, const float *sa, const void *qw, const float *sw, void *y,
                                 int64_t M, int64_t N, int64_t K, int num_groups, const int32_t *offsets,
-                                bool per_tensor, const DeviceInfo &dev, cudaStream_t stream) {
+                                ScaleMode mode, const DeviceInfo &dev, cudaStream_t stream) {
     const int bn = pick_bn(N);
-    if (per_tensor) {
-        if (bn == 256) return launch_variant<256, true>(qa, sa, qw, sw, y, M, N, K, num_groups, offsets, dev, stream);
-        return launch_variant<128, true>(qa, sa, qw, sw, y, M, N, K, num_groups, offsets, dev, stream);
-    }
-    if (bn == 256) return launch_variant<256, false>(qa, sa, qw, sw, y, M, N, K, num_groups, offsets, dev, stream);
-    return launch_variant<128, false>(qa, sa, qw, sw, y, M, N, K, num_groups, offsets, dev, stream);
+#define FP8_PREFILL_LAUNCH(MODE_)                                                                              \
+    return bn == 256 ? launch_variant<256, MODE_>(qa, sa, qw, sw, y, M, N, K, num_groups, offsets, dev, stream) \
+                     : launch_variant<128, MODE_>(qa, sa, qw, sw, y, M, N, K, num_groups, offsets, dev, stream)
+    if (mode == kScaleTensor) FP8_PREFILL_LAUNCH(kScaleTensor);
+    if (mode == kScaleRowCol) FP8_PREFILL_LAUNCH(kScaleRowCol);
+    FP8_PREFILL_LAUNCH(kScaleBlock);
+#undef FP8_PREFILL_LAUNCH
 }
 
 }  // namespace fp8k

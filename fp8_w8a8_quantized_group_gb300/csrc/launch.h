@@ -24,18 +24,36 @@ cudaError_t launch_quant_act_group(const void *x, void *q, float *s, int64_t M, 
                                    const DeviceInfo &dev, cudaStream_t stream);
 cudaError_t launch_quant_weight_block(const void *w, void *q, float *s, int64_t N, int64_t K,
                                       const DeviceInfo &dev, cudaStream_t stream);
+// One scale per row of x [rows][cols] (per-token activations, per-channel weights).
+cudaError_t launch_quant_rows(const void *x, void *q, float *s, int64_t rows, int64_t cols, const DeviceInfo &dev,
+                              cudaStream_t stream);
 cudaError_t launch_quant_per_tensor(const void *x, void *q, float *scale, int64_t n, bool is_static,
                                     const DeviceInfo &dev, cudaStream_t stream);
 
-// Tile-persistent tcgen05 GEMM (M > 16, or grouped). per_tensor: sa, sw point
-// to one float each and no per-block promotion is done.
+// How a GEMM applies the scales:
+//  kScaleBlock   sa [K/128][M], sw [ceil(N/128)][K/128]: promoted per 128-wide K block;
+//  kScaleTensor  sa, sw one float each: all of K accumulated, one product at the end;
+//  kScaleRowCol  sa [M] (per token), sw [N] (per output channel): all of K
+//                accumulated, Y[m,n] scaled by sa[m] * sw[n] at the end.
+enum ScaleMode : int { kScaleBlock = 0, kScaleTensor = 1, kScaleRowCol = 2 };
+
+// FP8 KV cache: quantize rows of key/value [tokens][elems] into cache slots
+// (store) or dequantize cache slots into rows (load), per-tensor scales.
+cudaError_t launch_kv_store(const void *key, const void *value, void *kc, void *vc, const int64_t *slots,
+                            const float *k_scale, const float *v_scale, int64_t tokens, int64_t elems,
+                            int64_t num_slots, const DeviceInfo &dev, cudaStream_t stream);
+cudaError_t launch_kv_load(const void *kc, const void *vc, void *key, void *value, const int64_t *slots,
+                           const float *k_scale, const float *v_scale, int64_t tokens, int64_t elems,
+                           int64_t num_slots, const DeviceInfo &dev, cudaStream_t stream);
+
+// Tile-persistent tcgen05 GEMM (M > 16, or grouped; grouped only with kScaleBlock).
 cudaError_t launch_gemm_prefill(const void *qa, const float *sa, const void *qw, const float *sw, void *y,
                                 int64_t M, int64_t N, int64_t K, int num_groups, const int32_t *offsets,
-                                bool per_tensor, const DeviceInfo &dev, cudaStream_t stream);
+                                ScaleMode mode, const DeviceInfo &dev, cudaStream_t stream);
 
 // Weight-streaming tcgen05 GEMM for M <= 16 (weights as the MMA's M side).
 cudaError_t launch_gemm_decode(const void *qa, const float *sa, const void *qw, const float *sw, void *y,
-                               int64_t M, int64_t N, int64_t K, bool per_tensor, const DeviceInfo &dev,
+                               int64_t M, int64_t N, int64_t K, ScaleMode mode, const DeviceInfo &dev,
                                cudaStream_t stream);
 
 // One CTA whose waits never complete: the first gives up after the wait limit

@@ -17,7 +17,7 @@
 //
 // The weight-block and per-tensor quantize passes are bound by instruction
 // issue; they reach the correctly rounded quotient's code through one
-// reciprocal per block or tensor (quant8_recip below), with a division only
+// reciprocal per block or tensor (quant8_recip in common.cuh), with a division only
 // near rounding boundaries. Codes are identical to quant8's either way.
 //
 // Every scale is fl32(max(amax, 1e-10) / 448) and every code
@@ -29,47 +29,8 @@
 namespace fp8k {
 namespace {
 
-// The E4M3 code pair of two FP32 values (low byte = a): the hardware's
-// round-to-nearest-even, saturating conversion.
-__device__ __forceinline__ uint32_t e4m3_pair(float a, float b) {
-    return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
-}
-
-// Same codes as quant8(v, s) - those of the correctly rounded quotients
-// RN(x/s) - for kernels bound by instruction issue, with r = RN(1/s)
-// computed once by the caller. q = RN(x*r) carries two roundings, so it lies
-// within 1.5 * 2^-23 |q| of RN(x/s), while RN(q * (1 -+ 2^-21)) lie more than
-// 3.5 * 2^-23 |q| away on either side: RN(x/s) lies between them. Rounding to
-// nearest even and saturating is monotonic, so when both bounds convert to
-// the codes of q, so does RN(x/s). Otherwise (near a rounding boundary of the
-// conversion), and whenever r overflows (s zero or subnormal, where x*r
-// could be 0 * Inf), the chunk takes correctly rounded divisions.
-__device__ __forceinline__ uint2 quant8_recip(const uint4 &v, float s, float r) {
-    const float x[8] = {bf16lo(v.x), bf16hi(v.x), bf16lo(v.y), bf16hi(v.y),
-                        bf16lo(v.z), bf16hi(v.z), bf16lo(v.w), bf16hi(v.w)};
-    constexpr float kDown = 1.0f - 0x1p-21f, kUp = 1.0f + 0x1p-21f;  // both exact in FP32
-    float q[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) q[i] = __fmul_rn(x[i], r);
-    uint2 out, lo, hi;
-    out.x = e4m3_pair(q[0], q[1]) | (e4m3_pair(q[2], q[3]) << 16);
-    out.y = e4m3_pair(q[4], q[5]) | (e4m3_pair(q[6], q[7]) << 16);
-    lo.x = e4m3_pair(__fmul_rn(q[0], kDown), __fmul_rn(q[1], kDown)) |
-           (e4m3_pair(__fmul_rn(q[2], kDown), __fmul_rn(q[3], kDown)) << 16);
-    lo.y = e4m3_pair(__fmul_rn(q[4], kDown), __fmul_rn(q[5], kDown)) |
-           (e4m3_pair(__fmul_rn(q[6], kDown), __fmul_rn(q[7], kDown)) << 16);
-    hi.x = e4m3_pair(__fmul_rn(q[0], kUp), __fmul_rn(q[1], kUp)) |
-           (e4m3_pair(__fmul_rn(q[2], kUp), __fmul_rn(q[3], kUp)) << 16);
-    hi.y = e4m3_pair(__fmul_rn(q[4], kUp), __fmul_rn(q[5], kUp)) |
-           (e4m3_pair(__fmul_rn(q[6], kUp), __fmul_rn(q[7], kUp)) << 16);
-    if ((lo.x != out.x) | (lo.y != out.y) | (hi.x != out.x) | (hi.y != out.y) | (fabsf(r) == INFINITY)) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) q[i] = __fdiv_rn(x[i], s);
-        out.x = e4m3_pair(q[0], q[1]) | (e4m3_pair(q[2], q[3]) << 16);
-        out.y = e4m3_pair(q[4], q[5]) | (e4m3_pair(q[6], q[7]) << 16);
-    }
-    return out;
-}
+// Error-word sites of the device-side argument checks.
+enum : unsigned { kSiteStaticScale = 301, kSiteStaticScaleSmall = 302 };
 
 // ------------------------------------------------ 1 x 128 activation groups --
 
@@ -94,12 +55,14 @@ __global__ void __launch_bounds__(kActThreads, 6) quant_act_group_kernel(const u
     const int lane = threadIdx.x & 31;
     const int c = lane & 3;
     const int64_t m = static_cast<int64_t>(blockIdx.x) * kActRows + (threadIdx.x >> 5);
-    const int64_t g = static_cast<int64_t>(blockIdx.y) * kActGroups + (lane >> 2);
     // Launched as a programmatic dependent: let the next kernel start its
-    // prologue, then wait for the kernel that produced x.
+    // prologue, then wait for the kernel that produced x. (A dependent that
+    // reads q or s before its own griddepcontrol.wait could see them half
+    // written; the GEMMs of this library read them only after it.)
     grid_dep_launch();
     grid_dep_wait();
 
+    const int64_t g = static_cast<int64_t>(blockIdx.y) * kActGroups + (lane >> 2);
     const bool ok = m < M && g < Kg;
     const int64_t base = m * K + g * 128 + c * 8;
     uint4 v[4];
@@ -179,6 +142,21 @@ __device__ __forceinline__ float block_reduce_max(float a, float *scratch) {
     return a;
 }
 
+// Bounds [c0, c1) of CTA b's share of n items split over g CTAs in equal
+// contiguous slices (the first n % g get one more), without forming n * b.
+__device__ __forceinline__ void slice_of(int64_t n, int64_t b, int64_t g, int64_t &c0, int64_t &c1) {
+    const int64_t q = n / g, r = n % g;
+    c0 = b * q + (b < r ? b : r);
+    c1 = c0 + q + (b < r ? 1 : 0);
+}
+
+// Device-side check of a caller's static scale: it must be positive and
+// finite. A bad one is recorded as FP8_ERR_ARG with `site` in the error word
+// (the quantization still runs, with that scale).
+__device__ __forceinline__ void check_static_scale(float sc, unsigned *err, unsigned site) {
+    if (!(sc > 0.0f && sc <= 3.402823466e38f)) record_error(err, kErrArg, site);
+}
+
 // amax of the whole tensor into *amax_bits (zeroed before): the bit pattern of
 // a non-negative float orders like the float, so atomicMax on it is a max.
 __global__ void __launch_bounds__(kTThreads) tensor_amax_kernel(const uint16_t *__restrict__ x, int64_t n8,
@@ -186,7 +164,8 @@ __global__ void __launch_bounds__(kTThreads) tensor_amax_kernel(const uint16_t *
     __shared__ float scratch[kTThreads / 32];
     grid_dep_launch();  // the quantize pass may be scheduled; it waits for this grid
     float a = 0.0f;
-    const int64_t c0 = n8 * blockIdx.x / gridDim.x, c1 = n8 * (blockIdx.x + 1) / gridDim.x;
+    int64_t c0, c1;
+    slice_of(n8, blockIdx.x, gridDim.x, c0, c1);
     for (int64_t i = c0 + threadIdx.x; i < c1; i += kTThreads * kTUnroll) {
         uint4 v[kTUnroll];
 #pragma unroll
@@ -203,17 +182,27 @@ __global__ void __launch_bounds__(kTThreads) tensor_amax_kernel(const uint16_t *
 
 // Quantize with the scale from the amax in *amax_bits (dynamic) or the scale
 // in *scale (static).
+//
+// Only the dynamic pass lets its dependent launch early: that dependent is the
+// finalize kernel, which waits for this grid before it touches anything. A
+// static call ends with this kernel, and what follows it on the stream may be
+// a decode GEMM that streams its weights before its own griddepcontrol.wait;
+// q may be those weights (a per-tensor weight quantized at load time), so the
+// static pass triggers only by completing.
 __global__ void __launch_bounds__(kTThreads) tensor_quant_kernel(const uint16_t *__restrict__ x,
                                                                  uint8_t *__restrict__ q, int64_t n8,
-                                                                 const float *scale, int from_amax) {
+                                                                 const float *scale, int from_amax,
+                                                                 unsigned *err) {
     // Launched as a programmatic dependent of the amax pass (or of whatever
     // precedes a static call): wait for it before reading the scale or x.
-    grid_dep_launch();
+    if (from_amax) grid_dep_launch();
     grid_dep_wait();
     const float stored = *scale;
     const float sc = from_amax ? block_scale(stored) : stored;
+    if (!from_amax && blockIdx.x == 0 && threadIdx.x == 0) check_static_scale(sc, err, kSiteStaticScale);
     const float rc = __frcp_rn(sc);
-    const int64_t c0 = n8 * blockIdx.x / gridDim.x, c1 = n8 * (blockIdx.x + 1) / gridDim.x;
+    int64_t c0, c1;
+    slice_of(n8, blockIdx.x, gridDim.x, c0, c1);
     for (int64_t i = c0 + threadIdx.x; i < c1; i += kTThreads * kTUnroll) {
         uint4 v[kTUnroll];
 #pragma unroll
@@ -262,11 +251,12 @@ cudaError_t launch_pdl(const void *fn, unsigned grid, unsigned block, void **arg
 // Whole per-tensor quantization in one CTA (small tensors).
 __global__ void __launch_bounds__(1024) tensor_quant_small_kernel(const uint16_t *__restrict__ x,
                                                                   uint8_t *__restrict__ q, int64_t n8,
-                                                                  float *scale, int is_static) {
+                                                                  float *scale, int is_static, unsigned *err) {
     __shared__ float scratch[32];
     float sc;
     if (is_static) {
         sc = *scale;
+        if (threadIdx.x == 0) check_static_scale(sc, err, kSiteStaticScaleSmall);
     } else {
         float a = 0.0f;
         for (int64_t i = threadIdx.x; i < n8; i += blockDim.x) a = fmaxf(a, amax8(ld_stream_v4(x + i * 8)));
@@ -277,7 +267,64 @@ __global__ void __launch_bounds__(1024) tensor_quant_small_kernel(const uint16_t
     if (!is_static && threadIdx.x == 0) *scale = sc;
 }
 
+// ---------------------------------------------------- one scale per row --
+
+constexpr int kRThreads = 256;
+constexpr int kRHeld = 8;  // 16-byte chunks of the row held in registers per thread
+
+// Row r of x [rows][cols] gets one scale from its own amax: per-token scales
+// for activations, per-channel scales for weights (rows = output channels).
+// One CTA per row (grid-stride); the first kRHeld * 256 chunks of the row stay
+// in registers between the amax and the quantize pass, any rest is read
+// again. Launched as a programmatic dependent, but lets nothing launch before
+// it completes: its codes may be the weights of a following decode GEMM.
+__global__ void __launch_bounds__(kRThreads) quant_rows_kernel(const uint16_t *__restrict__ x,
+                                                               uint8_t *__restrict__ q, float *__restrict__ s,
+                                                               int64_t rows, int64_t cols) {
+    __shared__ float scratch[kRThreads / 32];
+    grid_dep_wait();
+    const int64_t c8 = cols / 8;
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+        const uint16_t *xr = x + r * cols;
+        uint8_t *qr = q + r * cols;
+        uint4 v[kRHeld];
+        float a = 0.0f;
+#pragma unroll
+        for (int j = 0; j < kRHeld; ++j) {
+            const int64_t i = threadIdx.x + static_cast<int64_t>(j) * kRThreads;
+            v[j] = i < c8 ? ld_stream_v4(xr + i * 8) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int j = 0; j < kRHeld; ++j) a = fmaxf(a, amax8(v[j]));
+        for (int64_t i = threadIdx.x + kRHeld * kRThreads; i < c8; i += kRThreads) a = fmaxf(a, amax8(ld_stream_v4(xr + i * 8)));
+        a = block_reduce_max(a, scratch);
+        const float sc = block_scale(a);
+        const float rc = __frcp_rn(sc);
+#pragma unroll
+        for (int j = 0; j < kRHeld; ++j) {
+            const int64_t i = threadIdx.x + static_cast<int64_t>(j) * kRThreads;
+            if (i < c8) *reinterpret_cast<uint2 *>(qr + i * 8) = quant8_recip(v[j], sc, rc);
+        }
+        for (int64_t i = threadIdx.x + kRHeld * kRThreads; i < c8; i += kRThreads)
+            *reinterpret_cast<uint2 *>(qr + i * 8) = quant8_recip(ld_stream_v4(xr + i * 8), sc, rc);
+        if (threadIdx.x == 0) s[r] = sc;
+        __syncthreads();  // scratch is rewritten by the next row
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_quant_rows(const void *x, void *q, float *s, int64_t rows, int64_t cols, const DeviceInfo &dev,
+                              cudaStream_t stream) {
+    (void)dev;
+    if (rows == 0 || cols == 0) return cudaSuccess;
+    const int64_t grid = rows < 0x7FFFFFFF ? rows : 0x7FFFFFFF;
+    const uint16_t *xp = static_cast<const uint16_t *>(x);
+    uint8_t *qp = static_cast<uint8_t *>(q);
+    void *args[] = {&xp, &qp, &s, &rows, &cols};
+    return launch_pdl(reinterpret_cast<const void *>(quant_rows_kernel), static_cast<unsigned>(grid), kRThreads,
+                      args, stream);
+}
 
 cudaError_t launch_quant_act_group(const void *x, void *q, float *s, int64_t M, int64_t K,
                                    const DeviceInfo &dev, cudaStream_t stream) {
@@ -285,7 +332,7 @@ cudaError_t launch_quant_act_group(const void *x, void *q, float *s, int64_t M, 
     const int64_t rows = (M + kActRows - 1) / kActRows;
     const int64_t cols = (K / 128 + kActGroups - 1) / kActGroups;
     if (rows == 0 || cols == 0) return cudaSuccess;
-    if (rows > 0x7FFFFFFF || cols > 65535) return cudaErrorInvalidValue;
+    if (rows > 0x7FFFFFFF || cols > 65535) return cudaErrorInvalidValue;  // the entry point checks K first
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(rows), static_cast<unsigned>(cols));
     cfg.blockDim = dim3(kActThreads);
@@ -304,7 +351,7 @@ cudaError_t launch_quant_weight_block(const void *w, void *q, float *s, int64_t 
     (void)dev;
     const int64_t nb = (N + 127) / 128, kb = K / 128;
     if (nb == 0 || kb == 0) return cudaSuccess;
-    if (nb > 65535 || kb > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    if (nb > 65535 || kb > 0x7FFFFFFF) return cudaErrorInvalidValue;  // the entry point checks N first
     dim3 grid(static_cast<unsigned>(kb), static_cast<unsigned>(nb));
     quant_weight_block_kernel<<<grid, kWThreads, 0, stream>>>(static_cast<const uint16_t *>(w),
                                                               static_cast<uint8_t *>(q), s, N, K);
@@ -318,11 +365,11 @@ cudaError_t launch_quant_per_tensor(const void *x, void *q, float *scale, int64_
     uint8_t *qp = static_cast<uint8_t *>(q);
     if (n8 == 0) {
         if (is_static) return cudaSuccess;
-        tensor_quant_small_kernel<<<1, 32, 0, stream>>>(xp, qp, 0, scale, 0);
+        tensor_quant_small_kernel<<<1, 32, 0, stream>>>(xp, qp, 0, scale, 0, dev.err);
         return cudaGetLastError();
     }
     if (n <= kSmallTensor) {
-        tensor_quant_small_kernel<<<1, 1024, 0, stream>>>(xp, qp, n8, scale, is_static ? 1 : 0);
+        tensor_quant_small_kernel<<<1, 1024, 0, stream>>>(xp, qp, n8, scale, is_static ? 1 : 0, dev.err);
         return cudaGetLastError();
     }
     // Each pass runs as one resident wave, and the quantize and finalize
@@ -341,7 +388,8 @@ cudaError_t launch_quant_per_tensor(const void *x, void *q, float *scale, int64_
     const unsigned gq = static_cast<unsigned>(tensor_grid(tensor_quant_kernel, want, dev));
     int from_amax = is_static ? 0 : 1;
     const float *cscale = scale;
-    void *qargs[] = {&xp, &qp, const_cast<int64_t *>(&n8), &cscale, &from_amax};
+    unsigned *err = dev.err;
+    void *qargs[] = {&xp, &qp, const_cast<int64_t *>(&n8), &cscale, &from_amax, &err};
     cudaError_t e = launch_pdl(reinterpret_cast<const void *>(tensor_quant_kernel), gq, kTThreads, qargs, stream);
     if (e != cudaSuccess || is_static) return e;
     void *fargs[] = {&scale};

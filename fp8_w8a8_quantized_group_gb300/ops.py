@@ -158,6 +158,53 @@ def fp8_block_linear(x, qa, sa, qw, sw, y, stream=None) -> None:
     _check(_lib.load().fp8_block_linear(*args, M, N, K, _stream(stream)), "fp8_block_linear")
 
 
+def fp8_quant_rowwise(x, q, scales, stream=None) -> None:
+    rows, cols = x.shape
+    _need(q, rows * cols, "q")
+    _need(scales, rows, "scales")
+    args = _ptrs((x, torch.bfloat16, "x"), (q, CODES, "q"), (scales, torch.float32, "scales"))
+    _check(_lib.load().fp8_quant_rowwise(*args, rows, cols, _stream(stream)), "fp8_quant_rowwise")
+
+
+def fp8_rowwise_gemm(qa, sa, qw, sw, y, stream=None) -> None:
+    M, K = qa.shape
+    N = y.shape[1]
+    _need(sa, M, "sa")
+    _need(qw, N * K, "qw")
+    _need(sw, N, "sw")
+    _need(y, M * N, "y")
+    args = _ptrs((qa, CODES, "qa"), (sa, torch.float32, "sa"), (qw, CODES, "qw"), (sw, torch.float32, "sw"),
+                 (y, torch.bfloat16, "y"))
+    _check(_lib.load().fp8_rowwise_gemm(*args, M, N, K, _stream(stream)), "fp8_rowwise_gemm")
+
+
+def _kv_args(rows_a, rows_b, cache_a, cache_b, slot_mapping, k_scale, v_scale, rows_dtype):
+    T, E = rows_a.shape
+    S = cache_a.shape[0]
+    for t, n, what in ((rows_b, T * E, "value rows"), (cache_b, S * E, "value cache"), (cache_a, S * E, "key cache"),
+                       (slot_mapping, T, "slot_mapping"), (k_scale, 1, "k_scale"), (v_scale, 1, "v_scale")):
+        _need(t, n, what)
+    return T, E, S
+
+
+def fp8_kv_cache_store(key, value, key_cache, value_cache, slot_mapping, k_scale, v_scale, stream=None) -> None:
+    """key, value: BF16 [T, E]; caches: E4M3 [S, E]; slot_mapping: int64 [T]; scales: float32 [1]."""
+    T, E, S = _kv_args(key, value, key_cache, value_cache, slot_mapping, k_scale, v_scale, torch.bfloat16)
+    args = _ptrs((key, torch.bfloat16, "key"), (value, torch.bfloat16, "value"), (key_cache, CODES, "key_cache"),
+                 (value_cache, CODES, "value_cache"), (slot_mapping, torch.int64, "slot_mapping"),
+                 (k_scale, torch.float32, "k_scale"), (v_scale, torch.float32, "v_scale"))
+    _check(_lib.load().fp8_kv_cache_store(*args, T, E, S, _stream(stream)), "fp8_kv_cache_store")
+
+
+def fp8_kv_cache_load(key_cache, value_cache, key, value, slot_mapping, k_scale, v_scale, stream=None) -> None:
+    """Gather-and-dequantize: key, value (outputs) BF16 [T, E] from the caches' slots."""
+    T, E, S = _kv_args(key, value, key_cache, value_cache, slot_mapping, k_scale, v_scale, torch.bfloat16)
+    args = _ptrs((key_cache, CODES, "key_cache"), (value_cache, CODES, "value_cache"), (key, torch.bfloat16, "key"),
+                 (value, torch.bfloat16, "value"), (slot_mapping, torch.int64, "slot_mapping"),
+                 (k_scale, torch.float32, "k_scale"), (v_scale, torch.float32, "v_scale"))
+    _check(_lib.load().fp8_kv_cache_load(*args, T, E, S, _stream(stream)), "fp8_kv_cache_load")
+
+
 def fp8_status_string(status: int) -> str:
     return _lib.load().fp8_status_string(status).decode()
 
@@ -234,6 +281,21 @@ def block_linear(x, qw, sw, stream=None):
     y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
     fp8_block_linear(x, qa, sa, qw, sw, y, stream=stream)
     return y, qa, sa
+
+
+def quant_rowwise(x: torch.Tensor, stream=None):
+    """BF16 [R, C] -> (E4M3 codes uint8 [R, C], one scale per row float32 [R])."""
+    q = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    s = torch.empty((x.shape[0],), dtype=torch.float32, device=x.device)
+    fp8_quant_rowwise(x, q, s, stream=stream)
+    return q, s
+
+
+def rowwise_gemm(qa, sa, qw, sw, stream=None) -> torch.Tensor:
+    """Per-token x per-channel scaled GEMM -> BF16 [M, N]."""
+    y = torch.empty((qa.shape[0], qw.shape[0]), dtype=torch.bfloat16, device=qa.device)
+    fp8_rowwise_gemm(qa, sa, qw, sw, y, stream=stream)
+    return y
 
 
 def tensor_gemm(qa, sa, qw, sw, stream=None) -> torch.Tensor:

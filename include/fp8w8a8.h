@@ -34,13 +34,43 @@
  *  - The return value is a status (FP8_OK = 0). Argument errors are detected
  *    on the host before anything is enqueued. A zero M (or rows) is a valid
  *    no-op.
- *  - The quantizers by group and block, the GEMMs and fp8_block_linear take
- *    each of M, N, K (and N * num_groups when grouped) up to INT_MAX; larger
- *    values give FP8_ERR_SHAPE. fp8_quant_per_tensor takes any rows * cols
- *    that fits in half of the int64_t range.
+ *  - The GEMMs, fp8_block_linear and fp8_quant_rowwise take each of M, N, K
+ *    (and N * num_groups when grouped) up to INT_MAX; larger values give
+ *    FP8_ERR_SHAPE. fp8_quant_act_group takes K up to FP8_ACT_GROUP_MAX_K and
+ *    fp8_quant_weight_block N up to FP8_WEIGHT_BLOCK_MAX_N (the other size up
+ *    to INT_MAX). fp8_quant_per_tensor takes any rows * cols that fits in half
+ *    of the int64_t range.
  *  - Device-side waits in the kernels are bounded (about one second); if one
  *    expires the kernel stops early and records FP8_ERR_TIMEOUT, which
  *    fp8_device_error() reports. Kernels never trap.
+ *  - A few arguments can only be checked on the device (a static scale, the
+ *    grouped offsets): a bad one is recorded as FP8_ERR_ARG in the same error
+ *    word, the call still completes, and its outputs are unspecified.
+ *
+ * Programmatic dependent launch (PDL). Some kernels are launched as
+ * programmatic dependents of the work before them on the stream, and some
+ * let the next kernel launch before they complete (griddepcontrol.
+ * launch_dependents). A dependent always waits for its predecessor to
+ * complete before it reads that predecessor's outputs - with one exception:
+ * the decode GEMM (fp8_block_gemm dense, fp8_tensor_gemm, fp8_rowwise_gemm
+ * and fp8_block_linear, each with M <= 16) starts loading qw before that wait.
+ * So qw must not be written by a kernel that lets its dependents launch
+ * early. Per entry point:
+ *    fp8_quant_act_group     lets its dependent launch early (its q and s are
+ *                            written after that): never use its codes as the
+ *                            qw of a decode GEMM enqueued directly after it;
+ *    fp8_quant_weight_block  does not (qw from it is safe);
+ *    fp8_quant_per_tensor    does not, static or dynamic: its last kernel
+ *                            triggers only by completing (qw from it is safe);
+ *    fp8_quant_rowwise       does not (qw from it is safe);
+ *    decode GEMM             lets its dependent launch early; it writes y
+ *                            after its own wait, and reads only qw early;
+ *    prefill GEMM            does not;
+ *    fp8_block_linear        its quantizer lets its own GEMM launch early (the
+ *                            GEMM reads qa and sa after its wait); its GEMM is
+ *                            the decode or prefill GEMM above.
+ * Work that is not this library's (torch kernels, copies) never triggers
+ * early, so a plain stream order with it is always safe.
  */
 #ifndef FP8W8A8_H
 #define FP8W8A8_H
@@ -67,6 +97,10 @@ enum fp8_status {
 #define FP8_GROUP 128
 /* Largest num_groups accepted by fp8_block_gemm. */
 #define FP8_MAX_GROUPS 256
+/* Largest K of fp8_quant_act_group (65535 CTAs of 8 groups along K). */
+#define FP8_ACT_GROUP_MAX_K ((int64_t)65535 * 8 * FP8_GROUP)
+/* Largest N of fp8_quant_weight_block (65535 block rows). */
+#define FP8_WEIGHT_BLOCK_MAX_N ((int64_t)65535 * FP8_GROUP)
 
 /*
  * Dynamic activation quantization, one scale per token per 128-wide K group
@@ -105,12 +139,16 @@ int fp8_quant_weight_block(const void *w_bf16, void *q_e4m3, float *scales,
  *   x_bf16  [rows][cols] BF16, input.
  *   q_e4m3  [rows][cols] E4M3 codes, output.
  *   scale   ONE FP32 in device memory. is_static != 0: input, must hold a
- *           finite positive scale. is_static == 0: output, receives
- *           fl32(max(amax, 1e-10) / 448) of the whole tensor.
+ *           finite positive scale (checked on the device: otherwise
+ *           FP8_ERR_ARG, site 301 or 302, is recorded in the error word).
+ *           is_static == 0: output, receives fl32(max(amax, 1e-10) / 448) of
+ *           the whole tensor.
  *   cols must be a positive multiple of 16; rows >= 0.
  * A dynamic call enqueues up to four launches (zero the slot, amax, quantize,
  * write the scale); the scale slot holds the amax bit pattern in between, so
- * it must not be read by other work until the call's work is done.
+ * it must not be read by other work until the call's work is done. The last
+ * kernel of either mode lets nothing launch before it completes, so its codes
+ * may be the weights of a decode GEMM enqueued directly after it.
  * Errors: NULL, SHAPE, ALIGN, DEVICE, CUDA.
  */
 int fp8_quant_per_tensor(const void *x_bf16, void *q_e4m3, float *scale,
@@ -141,8 +179,12 @@ int fp8_quant_per_tensor(const void *x_bf16, void *q_e4m3, float *scale,
  * tile-persistent prefill kernel. The decode kernel is a programmatic
  * dependent of the work before it on `stream` and starts reading qw before
  * that work has completed: qw must not be written by a kernel that allows
- * its dependents to launch early (griddepcontrol.launch_dependents).
- * fp8_quant_weight_block never does; a plain stream order suffices.
+ * its dependents to launch early (see "Programmatic dependent launch" above;
+ * fp8_quant_weight_block and fp8_quant_per_tensor never do, so a plain stream
+ * order after them suffices).
+ * Offsets that are not non-decreasing within [0, M] are recorded as
+ * FP8_ERR_ARG (site 106) in the device error word; they are clamped into
+ * [0, M], so nothing is accessed outside the buffers.
  * Errors: NULL, SHAPE, ALIGN, UNSUPPORTED, ARG, DEVICE, CUDA.
  */
 int fp8_block_gemm(const void *qa, const float *sa, const void *qw, const float *sw,
@@ -158,11 +200,87 @@ int fp8_block_gemm(const void *qa, const float *sa, const void *qw, const float 
  *   sa, sw: ONE FP32 each, in DEVICE memory (as written by fp8_quant_per_tensor).
  *   K and N positive multiples of 16, M >= 0.
  * M <= 16 uses the decode kernel, with the same condition on qw as
- * fp8_block_gemm.
+ * fp8_block_gemm (fp8_quant_per_tensor, static or dynamic, satisfies it).
  * Errors: NULL, SHAPE, ALIGN, DEVICE, CUDA.
  */
 int fp8_tensor_gemm(const void *qa, const float *sa, const void *qw, const float *sw,
                     void *y_bf16, int64_t M, int64_t N, int64_t K, void *stream);
+
+/*
+ * Row-wise quantization: one scale per row of a BF16 matrix. For activations
+ * the rows are tokens (the dynamic per-token strategy, kFp8DynamicTokenSym,
+ * of "[vLLM] FP8", section "스케일링 전략 체계"); for weights the rows are
+ * output channels (the channel-wise weight scales of "서빙을 위한 양자화 가이드
+ * FP8, AWQ, GPTQ", section "연산까지 빨라지는 W8A8, FP8").
+ *
+ *   x_bf16  [rows][cols] BF16, input.
+ *   q_e4m3  [rows][cols] E4M3 codes, output.
+ *   scales  [rows] FP32, output: fl32(max(amax of the row, 1e-10) / 448).
+ *   cols a positive multiple of 16; rows >= 0.
+ * The kernel lets nothing launch before it completes, so its codes may be the
+ * weights of a decode GEMM enqueued directly after it.
+ * Errors: NULL, SHAPE, ALIGN, DEVICE, CUDA.
+ */
+int fp8_quant_rowwise(const void *x_bf16, void *q_e4m3, float *scales, int64_t rows, int64_t cols,
+                      void *stream);
+
+/*
+ * FP8 GEMM with per-token activation and per-channel weight scales:
+ *   Y[m,n] = bf16( sa[m] * sw[n] * sum_k dec(Qa[m,k]) dec(Qw[n,k]) ),
+ * FP32 accumulation over all of K, the scale product applied once at the end.
+ *
+ *   qa [M][K] E4M3 and sa [M] FP32 (as written by fp8_quant_rowwise on X).
+ *   qw [N][K] E4M3 and sw [N] FP32 (as written by fp8_quant_rowwise on W);
+ *   sw must be 16-byte aligned.
+ *   y  [M][N] BF16, output.
+ *   K and N positive multiples of 16, M >= 0.
+ * M <= 16 uses the decode kernel, with the same condition on qw as
+ * fp8_block_gemm (fp8_quant_rowwise satisfies it).
+ * Errors: NULL, SHAPE, ALIGN, DEVICE, CUDA.
+ */
+int fp8_rowwise_gemm(const void *qa, const float *sa, const void *qw, const float *sw,
+                     void *y_bf16, int64_t M, int64_t N, int64_t K, void *stream);
+
+/*
+ * FP8 KV cache, store: quantizes one step's keys and values into an E4M3
+ * cache with one FP32 scale per tensor for keys and one for values (the FP8
+ * KV cache of "[vLLM] FP8", section "KV 캐시 양자화", Fp8KVCacheMethod; the
+ * scales are 1.0 when no calibrated scale is given).
+ *
+ *   key_bf16, value_bf16   [num_tokens][token_elems] BF16, inputs
+ *                          (token_elems = KV heads * head dim).
+ *   key_cache, value_cache [num_slots][token_elems] E4M3, written at the slots
+ *                          below: cache[slot][e] = e4m3(fl32(x[t][e] / scale)).
+ *                          A paged cache addresses slot = block * block_size
+ *                          + offset (reading: slot-major layout).
+ *   slot_mapping           DEVICE int64 [num_tokens]: the slot of token t; a
+ *                          negative slot is padding and is skipped. A slot at
+ *                          or beyond num_slots is skipped and recorded as
+ *                          FP8_ERR_ARG (site 401) in the device error word.
+ *   k_scale, v_scale       ONE FP32 each in DEVICE memory, positive and finite
+ *                          (checked on the device: FP8_ERR_ARG, site 402).
+ *   token_elems a positive multiple of 16; num_tokens, num_slots >= 0.
+ * Distinct tokens must map to distinct slots (else the last writer is
+ * unspecified). Launched as a programmatic dependent; lets nothing launch
+ * before it completes.
+ * Errors: NULL, SHAPE, ALIGN (data 16 bytes, slot_mapping 8, scales 4),
+ * DEVICE, CUDA.
+ */
+int fp8_kv_cache_store(const void *key_bf16, const void *value_bf16, void *key_cache, void *value_cache,
+                       const int64_t *slot_mapping, const float *k_scale, const float *v_scale,
+                       int64_t num_tokens, int64_t token_elems, int64_t num_slots, void *stream);
+
+/*
+ * FP8 KV cache, load: gathers the cache slots of slot_mapping and
+ * dequantizes them to BF16 for attention: x[t][e] = bf16(fl32(dec(cache[slot][e])
+ * * scale)). Same arguments and rules as fp8_kv_cache_store, with the caches
+ * as inputs and key_bf16 / value_bf16 as outputs; rows of skipped tokens are
+ * not written.
+ * Errors: NULL, SHAPE, ALIGN, DEVICE, CUDA.
+ */
+int fp8_kv_cache_load(const void *key_cache, const void *value_cache, void *key_bf16, void *value_bf16,
+                      const int64_t *slot_mapping, const float *k_scale, const float *v_scale,
+                      int64_t num_tokens, int64_t token_elems, int64_t num_slots, void *stream);
 
 /*
  * W8A8 linear layer, Y = X * W^T, from BF16 activations: dynamic 1x128
@@ -190,9 +308,10 @@ const char *fp8_status_string(int status);
 
 /*
  * Synchronises `stream`, then reads and clears the current device's error
- * word, which kernels set when a bounded wait expires. *out_code receives
- * FP8_OK or FP8_ERR_TIMEOUT; *out_site (may be NULL) a number naming the wait
- * that expired. Returns FP8_OK; FP8_ERR_NULL if out_code is NULL (checked
+ * word, which kernels set when a bounded wait expires or a device-checked
+ * argument is bad (the first such event since the last read is kept).
+ * *out_code receives FP8_OK, FP8_ERR_TIMEOUT or FP8_ERR_ARG; *out_site (may
+ * be NULL) a number naming the wait or the check. Returns FP8_OK; FP8_ERR_NULL if out_code is NULL (checked
  * first, on the host); FP8_ERR_DEVICE if the current device is not sm_103;
  * FP8_ERR_CUDA if the synchronisation or the read failed (e.g. an earlier
  * kernel faulted).

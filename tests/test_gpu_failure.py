@@ -53,3 +53,39 @@ def test_context_usable_after_an_expired_wait():
     assert np.array_equal(q.cpu().numpy(), qo)
     assert np.array_equal(f32_bits(s.cpu().numpy()), f32_bits(so))
     assert ops.fp8_device_error() == (0, 0)
+
+
+FP8_ERR_ARG = 5
+
+
+@pytest.mark.parametrize("bad", [0.0, -0.5, float("nan"), float("inf")])
+@pytest.mark.parametrize("rows,site", [(8, 302), (2048, 301)])  # single-CTA and multi-kernel paths
+def test_bad_static_scale_is_reported(bad, rows, site):
+    """A static per-tensor scale must be positive and finite; only the device
+    can read it, so a bad one is recorded in the error word."""
+    x = synth.device_normal_bf16(rows, 256, 0, "failure/static")
+    q = torch.empty((rows, 256), dtype=torch.uint8, device="cuda")
+    s = torch.tensor([bad], dtype=torch.float32, device="cuda")
+    assert ops.fp8_device_error() == (0, 0)
+    ops.fp8_quant_per_tensor(x, q, s, True)
+    assert ops.fp8_device_error() == (FP8_ERR_ARG, site)
+    ops.fp8_quant_per_tensor(x, q, torch.tensor([0.01], device="cuda"), True)
+    assert ops.fp8_device_error() == (0, 0)
+
+
+@pytest.mark.parametrize("offsets", [[0, 40, 30, 64], [-1, 20, 40, 64], [0, 20, 40, 65], [10, 5, 40, 64]])
+def test_bad_group_offsets_are_reported(offsets):
+    """Grouped offsets must be non-decreasing within [0, M]; the kernel clamps
+    them (no access leaves the buffers) and records FP8_ERR_ARG, site 106."""
+    M, N, K, E = 64, 128, 256, 3
+    qa = torch.zeros((M, K), dtype=torch.uint8, device="cuda")
+    sa = torch.ones((K // 128, M), dtype=torch.float32, device="cuda")
+    qw = torch.zeros((E, N, K), dtype=torch.uint8, device="cuda")
+    sw = torch.ones((E, N // 128, K // 128), dtype=torch.float32, device="cuda")
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    good = torch.tensor([0, 20, 40, 64], dtype=torch.int32, device="cuda")
+    ops.fp8_block_gemm(qa, sa, qw, sw, y, num_groups=E, group_offsets=good)
+    assert ops.fp8_device_error() == (0, 0)
+    bad = torch.tensor(offsets, dtype=torch.int32, device="cuda")
+    ops.fp8_block_gemm(qa, sa, qw, sw, y, num_groups=E, group_offsets=bad)
+    assert ops.fp8_device_error() == (FP8_ERR_ARG, 106)

@@ -305,3 +305,43 @@ def test_block_linear_repeated_calls_stable():
     qw, sw = ops.quant_weight_block(to_dev_bf16(w))
     outs = [ops.block_linear(xd, qw, sw)[0] for _ in range(3)]
     assert all(torch.equal(o.view(torch.int16), outs[0].view(torch.int16)) for o in outs[1:])
+
+
+# -------------------------------------------- per token x per channel --
+
+@pytest.mark.parametrize("rows,cols", [(1, 4096), (16, 14336), (7, 272), (300, 1040), (2048, 4096), (5, 20480)])
+def test_quant_rowwise_bit_exact(rows, cols):
+    x = synth.activations(rows, cols, 6, f"rowq/{rows}x{cols}")
+    q, s = ops.quant_rowwise(to_dev_bf16(x))
+    qo, so = oracle.quant_rowwise(x)
+    assert np.array_equal(f32_bits(s.cpu().numpy()), f32_bits(so))
+    assert np.array_equal(q.cpu().numpy(), qo)
+
+
+def _rowwise_case(M, N, K, seed):
+    x, w = synth.block_case(M, N, K, seed=seed)
+    qa, sa = ops.quant_rowwise(to_dev_bf16(x))
+    qw, sw = ops.quant_rowwise(to_dev_bf16(w))
+    qao, sao = oracle.quant_rowwise(x)
+    qwo, swo = oracle.quant_rowwise(w)
+    assert np.array_equal(qa.cpu().numpy(), qao) and np.array_equal(f32_bits(sa.cpu().numpy()), f32_bits(sao))
+    assert np.array_equal(qw.cpu().numpy(), qwo) and np.array_equal(f32_bits(sw.cpu().numpy()), f32_bits(swo))
+    return (qa, sa, qw, sw), (qao, sao, qwo, swo)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 256, 256), (16, 1024, 2048), (5, 272, 208), (3, 19584, 768),
+                                   (17, 256, 256), (300, 512, 1040), (129, 384, 512)])
+def test_rowwise_gemm_full_compare(M, N, K):
+    (qa, sa, qw, sw), (qao, sao, qwo, swo) = _rowwise_case(M, N, K, seed=12)
+    y = ops.rowwise_gemm(qa, sa, qw, sw)
+    yo, ab = oracle.gemm_rowwise(qao, sao, qwo, swo)
+    assert_within_tolerance(bf16_to_f64(y), yo, ab, f"rowwise {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 28672, 4096), (16, 4096, 14336), (2048, 4096, 4096), (4096, 6144, 4096)])
+def test_rowwise_gemm_full_size(M, N, K):
+    (qa, sa, qw, sw), (qao, sao, qwo, swo) = _rowwise_case(M, N, K, seed=13)
+    yg = bf16_to_f64(ops.rowwise_gemm(qa, sa, qw, sw))
+    ms, ns = _sample_points(M, N, n_random=3000)
+    yo, ab = oracle.gemm_rowwise_points(qao, sao, qwo, swo, ms, ns)
+    assert_within_tolerance(yg[ms, ns], yo, ab, f"rowwise {M}x{N}x{K} sampled")
