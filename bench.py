@@ -271,18 +271,28 @@ def decode_calls():
 def run_decode_section(torch, ops, dev, steps, warmup, peaks, sync_ranks):
     layers, acts = build_decode(torch, ops, dev)
     calls = decode_calls()
+    ws = ops.fused_workspace(dev)  # the grid barrier's words, one per stream
 
     def step(marks):
         for (M, layer, i) in calls:
             N, K = SHAPES[i]
             x, qa, sa, ys = acts[(M, N, K)]
             qw, sw = layers[layer][i]
+            ops.fp8_block_linear_fused(x, qa, sa, qw, sw, ys[layer], ws)
+
+    def step_two_kernels(marks):
+        for (M, layer, i) in calls:
+            N, K = SHAPES[i]
+            x, qa, sa, ys = acts[(M, N, K)]
+            qw, sw = layers[layer][i]
             ops.fp8_block_linear(x, qa, sa, qw, sw, ys[layer])
 
-    timed = Timed(torch, step)
-    ms, window = time_steps(torch, timed.replay, steps, warmup, sync_ranks)
     step_bytes = sum(linear_bytes(M, *SHAPES[i]) for M, _, i in calls)
     gemm_total_bytes = sum(gemm_bytes(M, *SHAPES[i]) for M, _, i in calls)
+    timed2 = Timed(torch, step_two_kernels)
+    ms2, _ = time_steps(torch, timed2.replay, steps, warmup)
+    timed = Timed(torch, step)
+    ms, window = time_steps(torch, timed.replay, steps, warmup, sync_ranks)
     value = step_bytes * steps / (ms * 1e-3) / 1e9
 
     # Dominant kernel: the same GEMM launches back to back in one graph (the
@@ -316,7 +326,9 @@ def run_decode_section(torch, ops, dev, steps, warmup, peaks, sync_ranks):
             us = t * 1e3 / (reps * LAYERS)
             per_shape[f"M{M}_N{N}_K{K}"] = {"us": us, "GBps": gemm_bytes(M, N, K) / (us * 1e-6) / 1e9}
     out = {"value": value, "ms_per_step": ms / steps, "roofline": roof, "per_shape": per_shape,
-           "launches_per_step": 2 * len(calls), "window": window, "step_bytes": step_bytes}
+           "launches_per_step": len(calls), "window": window, "step_bytes": step_bytes,
+           "two_kernel_path": {"value": step_bytes * steps / (ms2 * 1e-3) / 1e9, "ms_per_step": ms2 / steps,
+                               "note": "the same step through fp8_block_linear (quantizer kernel + GEMM kernel)"}}
 
     # End to end through the C entry point, as a C caller drives it: the step's
     # 96 activation inputs sit in one pinned host slab and its 96 outputs
@@ -345,14 +357,15 @@ def run_decode_section(torch, ops, dev, steps, warmup, peaks, sync_ranks):
     d2h = y_host.numel() * 2
     stream = torch.cuda.current_stream()
     handle = stream.cuda_stream
-    linear = lib.fp8_block_linear
+    linear = lib.fp8_block_linear_fused
+    ws_ptr, ws_bytes = ws.data_ptr(), ws.numel() * 4
 
     def e2e_step():
         x_dev.copy_(x_host, non_blocking=True)
         for a in args:
-            st = linear(*a, handle)
+            st = linear(*a, ws_ptr, ws_bytes, handle)
             if st:
-                raise RuntimeError(f"fp8_block_linear: status {st}")
+                raise RuntimeError(f"fp8_block_linear_fused: status {st}")
         y_host.copy_(y_dev, non_blocking=True)
 
     e2e_steps = max(1, min(steps, 20))
@@ -360,8 +373,9 @@ def run_decode_section(torch, ops, dev, steps, warmup, peaks, sync_ranks):
     out["e2e"] = {"value": step_bytes * e2e_steps / (ms_e2e * 1e-3) / 1e9, "unit": "GB/s",
                   "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                   "ms_per_step": ms_e2e / e2e_steps,
-                  "note": "eager C-ABI calls (no graph); per step one pinned host->device copy of the 96 "
-                          "inputs and one device->host copy of the 96 outputs, on the compute stream"}
+                  "note": "eager C-ABI calls of fp8_block_linear_fused (no graph); per step one pinned "
+                          "host->device copy of the 96 inputs and one device->host copy of the 96 outputs, on the "
+                          "compute stream"}
     del layers, acts
     return out
 
@@ -458,11 +472,15 @@ def run_tensor_section(torch, ops, dev, steps, warmup, peaks):
 
 
 def run_moe_section(torch, ops, dev, steps, warmup, peaks):
+    """Mixture-of-experts layer: 8 experts [2048, 7168], 4096 tokens routed
+    top-2 (8192 rows). Timed: activation quantization of the tokens in token
+    order + the grouped GEMM that gathers each routed row (row-gather TMA);
+    also the GEMM alone, and the older route through a permuted copy."""
     tokens, E, N, K = 4096, 8, 2048, 7168
     token_of_row, offsets = synth.route_top2(tokens, E, seed=0)
     x = synth.device_normal_bf16(tokens, K, 0, "bench/moe/X", device=dev)
-    xp = x.index_select(0, torch.from_numpy(token_of_row).to(dev))  # routing gather (harness, untimed)
-    del x
+    ri = torch.from_numpy(token_of_row.astype(np.int32)).to(dev)
+    xp = x.index_select(0, torch.from_numpy(token_of_row).to(dev))  # the permuted copy (older route, untimed)
     qw = torch.empty((E, N, K), dtype=torch.uint8, device=dev)
     sw = torch.empty((E, N // 128, K // 128), dtype=torch.float32, device=dev)
     for e in range(E):
@@ -487,11 +505,37 @@ def run_moe_section(torch, ops, dev, steps, warmup, peaks):
     timed = Timed(torch, step, n_marks=1)
     time_steps(torch, timed.replay, steps, warmup)
     out = {"counts": np.diff(offsets).tolist()}
+    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+    fl = 2.0 * M * N * K
     if timed.ext:
         t = timed.mark_ms()[0] * 1e-3
-        fl = 2.0 * M * N * K
-        out.update({"us": t * 1e6, "TFLOPS": fl / t / 1e12,
-                    "frac_fp8_peak": fl / t / 1e12 / (peaks["bf16_tflops"] * FP8_OVER_BF16)})
+        out["permuted_copy"] = {"gemm_us": t * 1e6, "TFLOPS": fl / t / 1e12, "frac_fp8_peak": fl / t / 1e12 / fp8_peak}
+    qt = torch.empty((tokens, K), dtype=torch.uint8, device=dev)
+    st = torch.empty((K // 128, tokens), dtype=torch.float32, device=dev)
+
+    def step_gather(marks):
+        flush.zero_()
+        if marks:
+            marks[0][0].record()
+        ops.fp8_quant_act_group(x, qt, st)
+        if marks:
+            marks[1][0].record()
+        ops.fp8_block_gemm_gather(qt, st, ri, qw, sw, y, off)
+        if marks:
+            marks[0][1].record()
+            marks[1][1].record()
+    tg = Timed(torch, step_gather, n_marks=2)
+    ms, _ = time_steps(torch, tg.replay, steps, warmup)
+    if tg.ext:
+        t_all, t_gemm = (v * 1e-3 for v in tg.mark_ms())
+        out.update({"us": t_gemm * 1e6, "TFLOPS": fl / t_gemm / 1e12, "frac_fp8_peak": fl / t_gemm / 1e12 / fp8_peak,
+                    "layer_us": t_all * 1e6, "layer_TFLOPS": fl / t_all / 1e12,
+                    "roofline": {"bound": "tensor", "achieved": fl / t_gemm / 1e12, "peak": fp8_peak,
+                                 "unit": "TFLOP/s", "frac": fl / t_gemm / 1e12 / fp8_peak,
+                                 "peak_source": f"bf16_tflops of {peaks['source']} x {FP8_OVER_BF16}"},
+                    "note": "TFLOPS of the row-gather grouped GEMM; layer_* = token-order activation "
+                            "quantization + that GEMM, after a 256 MB L2 flush"})
+    del x, xp
     return out
 
 
@@ -640,40 +684,52 @@ def run_kv_section(torch, ops, dev, steps, warmup, peaks):
 
 # --------------------------------------------------------------- CPU legs --
 
-def oracle_decode_sample(budget_s: float):
-    """Times the CPU oracle on a bounded sample of the decode workload: for each
-    projection at M = 1, activation quantization of X [1, K] and the FP64 GEMM
-    on the first n columns, n chosen to fit the time budget. Returns
-    (GB/s of algorithmic bytes, description)."""
+_CPU_WEIGHTS = {}
+
+
+def _cpu_weights(N, K, n):
+    """Quantized weights of the first n rows of a projection for the CPU legs
+    (generated and quantized once per process, outside every timed region)."""
+    import oracle
+    key = (N, K, n)
+    if key not in _CPU_WEIGHTS:
+        _CPU_WEIGHTS[key] = oracle.quant_weight_block(synth.weights(n, K, 0, f"cpu/W/{N}x{K}"))
+    return _CPU_WEIGHTS[key]
+
+
+def oracle_decode_sample(threads: int | None = None, ms=None, cols: int | None = None):
+    """Times the CPU oracle on one layer of the decode workload: for each M in
+    `ms` and each projection, activation quantization of X [M, K] and the FP64
+    dequantize-then-GEMM over the first `cols` output columns (all N by
+    default). `threads` host threads split the output columns at 128-column
+    boundaries (the oracle's C calls release the GIL). Returns (GB/s of
+    algorithmic bytes, description, seconds)."""
+    import concurrent.futures as cf
+
     import oracle
     oracle.build()
-    frac = 1.0
-    # calibrate on a small slice
-    x = synth.activations(1, 4096, 0, "cpu/X/4096")
-    w = synth.weights(256, 4096, 0, "cpu/W/calib")
-    qa, sa = oracle.quant_act_group(x)
-    qw, sw = oracle.quant_weight_block(w)
-    t0 = time.perf_counter()
-    oracle.gemm_block_points(qa, sa, qw, sw, np.zeros(256, np.int64), np.arange(256))
-    per_mac = (time.perf_counter() - t0) / (256 * 4096)
-    total_macs = sum(N * K for N, K in SHAPES)
-    frac = min(1.0, budget_s / max(per_mac * total_macs, 1e-9))
-    nbytes = 0.0
-    t_total = 0.0
-    cols_used = []
-    for (N, K) in SHAPES:
-        n = max(128, int(N * frac) // 128 * 128)
-        x = synth.activations(1, K, 0, f"cpu/X/{K}")
-        w = synth.weights(n, K, 0, f"cpu/W/{N}x{K}")
-        qw, sw = oracle.quant_weight_block(w)  # offline step, not timed
-        t0 = time.perf_counter()
-        qa, sa = oracle.quant_act_group(x)
-        oracle.gemm_block_points(qa, sa, qw, sw, np.zeros(n, np.int64), np.arange(n))
-        t_total += time.perf_counter() - t0
-        nbytes += linear_bytes(1, n, K)
-        cols_used.append(n)
-    desc = (f"M=1 decode: activation quantization + FP64 GEMM on the first {cols_used} output columns of the "
-            f"four projections (one layer), single-threaded C oracle")
+    threads = threads or os.cpu_count() or 1
+    ms = list(ms or DECODE_M)
+    cases = [(N, K, min(N, cols) if cols else N) for (N, K) in SHAPES]
+    xs = {(M, K): synth.activations(M, K, 0, f"cpu/X/{M}x{K}") for M in ms for (_, K, _) in cases}
+    t_total, nbytes = 0.0, 0.0
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        for M in ms:
+            for (N, K, n) in cases:
+                qw, sw = _cpu_weights(N, K, n)
+                blocks = -(-n // 128)
+                bounds = [128 * (blocks * i // threads) for i in range(threads + 1)]
+                bounds[-1] = n
+                t0 = time.perf_counter()
+                qa, sa = oracle.quant_act_group(xs[(M, K)])
+                futs = [ex.submit(oracle.gemm_block, qa, sa, qw[a:b], sw[a // 128:-(-b // 128)], with_absdot=False)
+                        for a, b in zip(bounds[:-1], bounds[1:]) if b > a]
+                for f in futs:
+                    f.result()
+                t_total += time.perf_counter() - t0
+                nbytes += linear_bytes(M, n, K)
+    desc = (f"one layer of the decode step: M in {ms} x the four projections, activation quantization + FP64 GEMM "
+            f"on the first {[n for (_, _, n) in cases]} output columns, C oracle on {threads} host thread(s)")
     return nbytes / t_total / 1e9, desc, t_total
 
 
@@ -703,20 +759,21 @@ def reference_arm(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    per_step_budget = max(0.5, 120.0 / max(1, args.steps + args.warmup))
     vals = []
     desc = ""
+    threads = os.cpu_count() or 1
     for i in range(args.warmup + args.steps):
-        v, desc, _ = oracle_decode_sample(per_step_budget)
+        v, desc, _ = oracle_decode_sample(threads)
         if i >= args.warmup:
             vals.append(v)
     value = statistics.median(vals)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded SplitMix64/Box-Muller)",
-            "config": {"workload": decode_workload(), "parallelism": "host, one thread",
-                       "sample": "each step a bounded sample of the workload (cpu_baseline.sample)"},
-            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc,
+            "config": {"workload": decode_workload(), "parallelism": f"host, {threads} threads",
+                       "sample": "each step one layer of the workload (cpu_baseline.sample), the same sample "
+                                 "as the GPU arm's cpu_baseline"},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": desc,
                              "host": host_cpu()},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
@@ -726,7 +783,7 @@ def reference_arm(args):
 
 def run_case(spec: str, launches: int):
     """One kernel on one shape, for profiling: KIND:M:N:K with KIND in
-    decode|prefill|linear|tensor|moe|act|weight|ptensor. Prints per-launch times."""
+    decode|prefill|linear|fused|tensor|moe|act|weight|ptensor. Prints per-launch times."""
     import torch
 
     import __graft_entry__
@@ -748,6 +805,13 @@ def run_case(spec: str, launches: int):
         qw, sw = ops.quant_weight_block(synth.device_normal_bf16(N, K, 0, "case/W", sigma=0.02, device=dev))
         y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
         fn = lambda: ops.fp8_block_linear(x, qa, sa, qw, sw, y)  # noqa: E731
+    elif kind == "fused":
+        qa = torch.empty((M, K), dtype=torch.uint8, device=dev)
+        sa = torch.empty((K // 128, M), dtype=torch.float32, device=dev)
+        qw, sw = ops.quant_weight_block(synth.device_normal_bf16(N, K, 0, "case/W", sigma=0.02, device=dev))
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        ws = ops.fused_workspace(dev)
+        fn = lambda: ops.fp8_block_linear_fused(x, qa, sa, qw, sw, y, ws)  # noqa: E731
     elif kind == "tensor":
         qa, sa = ops.quant_per_tensor(x)
         qw, sw = ops.quant_per_tensor(synth.device_normal_bf16(N, K, 0, "case/W", sigma=0.02, device=dev))
@@ -809,7 +873,6 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--sections", default="prefill,tensor,moe,quant,rowwise,kv")
-    ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--case", default=None, help="profile one kernel: KIND:M:N:K")
     ap.add_argument("--launches", type=int, default=3)
     args = ap.parse_args()
@@ -867,9 +930,12 @@ def main():
         return
     cpu = None
     if world == 1:
-        v, desc, secs = oracle_decode_sample(args.cpu_budget)
-        cpu = {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc,
-               "seconds": round(secs, 2), "host": host_cpu()}
+        threads = os.cpu_count() or 1
+        v, desc, secs = oracle_decode_sample(threads)
+        v1, desc1, secs1 = oracle_decode_sample(1, ms=[1])
+        cpu = {"value": v, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": desc,
+               "seconds": round(secs, 2), "host": host_cpu(),
+               "one_core": {"value": v1, "sample": desc1, "seconds": round(secs1, 2)}}
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",

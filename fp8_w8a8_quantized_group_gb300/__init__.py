@@ -9,8 +9,12 @@ from .ops import (  # noqa: F401
     Fp8Error,
     block_gemm,
     block_linear,
+    block_linear_fused,
+    fused_workspace,
     fp8_block_gemm,
+    fp8_block_gemm_gather,
     fp8_block_linear,
+    fp8_block_linear_fused,
     fp8_device_error,
     fp8_kv_cache_load,
     fp8_kv_cache_store,

@@ -54,16 +54,27 @@ constexpr int kScaleKb = 8;     // K blocks of activation/weight scales staged a
 constexpr int kScaleBytes = 4 * 4 * (kScaleKb * kTok + kScaleKb);
 constexpr int kRecvBytes = kRows * kTok * 4;  // split-K partials addressed to this CTA
 constexpr int kSmemBytes =
-    1024 + kStages * (kWBytes + kXBytes) + kRecvBytes + 8 * (2 * kStages + 5) + 16 + kScaleBytes;
+    1024 + kStages * (kWBytes + kXBytes) + kRecvBytes + 8 * (2 * kStages + 6) + 16 + kScaleBytes;
 
 enum : unsigned { kSiteProdEmpty = 201, kSiteMmaTmem = 202, kSiteMmaFull = 203, kSiteEpiFull = 204,
-                  kSiteDrain = 205, kSiteReduce = 206 };
+                  kSiteDrain = 205, kSiteReduce = 206, kSiteGridSync = 207, kSiteQuantReady = 208 };
 
-template <int MODE>
+// Optional fused activation quantization (block mode only): x is the BF16
+// input [M][K], the activation codes go to the tensor `tmX` maps (qa_out) and
+// the scales to sa, and ws is the grid barrier's two words.
+struct FusedQuant {
+    const uint16_t *x;
+    uint8_t *qa_out;
+    unsigned *ws;
+};
+
+template <int MODE, bool FUSED>
 __global__ void __launch_bounds__(kThreads, 2)
     gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                        const float *__restrict__ sa, const float *__restrict__ sw,
-                       __nv_bfloat16 *__restrict__ y, int M, int N, int K, int splits, unsigned *err) {
+                       __nv_bfloat16 *__restrict__ y, int M, int N, int K, int splits, unsigned *err,
+                       FusedQuant fq) {
+    static_assert(!FUSED || MODE == kScaleBlock, "fused activation quantization is block-scaled");
     constexpr bool WHOLE_K = MODE != kScaleBlock;  // all of the CTA's K in one TMEM accumulator
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -75,7 +86,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint64_t *tfull = empty + kStages;
     uint64_t *tempty = tfull + 2;
     uint64_t *rbar = tempty + 2;  // completes when all kRecvBytes have arrived
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(rbar + 1);
+    uint64_t *qready = rbar + 1;  // fused: every CTA's activation codes are in memory
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(qready + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     float *scale_smem = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(tmem_slot) + 16);
 
@@ -91,6 +103,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
         for (int b = 0; b < 2; ++b) { mbar_init(&tfull[b], 1); mbar_init(&tempty[b], 128); }
         mbar_init(rbar, 1);
+        mbar_init(qready, 1);
         *abort_flag = 0;
         fence_barrier_init();
         if (splits > 1) mbar_arrive_expect_tx(rbar, kRecvBytes);
@@ -130,6 +143,16 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int i = pre; i < warm; ++i) tma_prefetch_l2_2d(&tmW, (kb0 + i) * BK, n0);
             if (splits > 1) cluster_wait_acquire();
             grid_dep_wait();
+            if (FUSED) {
+                // The activation codes are written by the CTAs of this grid
+                // (generic stores) and read here by TMA: wait until every CTA
+                // has passed the grid barrier, then order the async-proxy
+                // reads after it. The loads are issued even if the wait gave
+                // up (the codes are then stale, and the error is recorded), so
+                // that every stage still completes and drains.
+                mbar_wait(qready, 0, abort_flag, err, kSiteQuantReady);
+                fence_proxy_async_global();
+            }
             for (int i = 0; i < pre; ++i) tma_load_2d(sX + i * kXBytes, &tmX, &full[i], (kb0 + i) * BK, 0);
             uint32_t stage = static_cast<uint32_t>(pre % kStages), phase = pre == kStages ? 1u : 0u;
             int issued = pre;
@@ -198,6 +221,29 @@ __global__ void __launch_bounds__(kThreads, 2)
         const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(ep * 32) << 16);
         uint32_t buf = 0, bphase = 0;
         grid_dep_wait();
+        if (FUSED) {
+            // Fused activation quantization: the grid's CTAs take equal
+            // contiguous shares of the M x K/128 activation groups (in (row,
+            // group) order), a lane quad per group as in the stand-alone
+            // quantizer, and meet at a grid barrier before any CTA reads the
+            // codes. Every group is quantized exactly once.
+            const int64_t G = static_cast<int64_t>(M) * Kg;
+            const int64_t g0 = G * blockIdx.x / gridDim.x, g1 = G * (blockIdx.x + 1) / gridDim.x;
+            const int quad = (ep * 32 + lane) >> 2;
+            for (int64_t base = g0; base < g1; base += 32) {  // the same trip count in all four warps
+                const int64_t gi = base + quad;
+                const bool ok = gi < g1;
+                const int64_t m = ok ? gi / Kg : 0;
+                quant_group_by_quad(fq.x, fq.qa_out, const_cast<float *>(sa), M, K, m, ok ? gi - m * Kg : 0,
+                                    lane & 3, ok, [](const uint16_t *p) { return ld_stream_v4(p); });
+            }
+            named_bar_sync(2, 128);
+            if (ep == 0 && lane == 0) {
+                grid_barrier(fq.ws, gridDim.x, abort_flag, err, kSiteGridSync);
+                mbar_arrive(qready);
+            }
+            named_bar_sync(2, 128);
+        }
         if (!WHOLE_K) {
             // Scales of kScaleKb K blocks at a time go through this warp's own
             // shared-memory slice; the next chunk is loaded into registers while
@@ -211,7 +257,10 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                 for (int i = 0; i < kScaleKb * kTok / 32; ++i) {
                     const int idx = lane + 32 * i;
-                    r_sa[i] = idx < n * M ? __ldg(sa + static_cast<int64_t>(c0) * M + idx) : 0.0f;
+                    const float *p = sa + static_cast<int64_t>(c0) * M + idx;
+                    // fused: sa is written by other CTAs of this grid, so not
+                    // through the read-only path
+                    r_sa[i] = idx < n * M ? (FUSED ? ld_cg_f32(p) : __ldg(p)) : 0.0f;
                 }
                 r_sw = lane < n ? __ldg(swrow + c0 + lane) : 0.0f;
             };
@@ -354,30 +403,40 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 }
 
-template <int MODE>
-cudaError_t launch_variant(const void *qa, const float *sa, const void *qw, const float *sw, void *y, int64_t M,
-                           int64_t N, int64_t K, const DeviceInfo &dev, cudaStream_t stream) {
+// Split of K over a cluster: as far as all CTAs still fit on the GPU at once
+// (two per SM), so that no CTA waits for a second wave.
+int pick_splits(int64_t N, int64_t K, const DeviceInfo &dev) {
+    const int64_t nblocks = (N + kRows - 1) / kRows;
+    const int64_t Kg = (K + BK - 1) / BK;
+    int splits = 1;
+    while (splits < 8 && nblocks * splits * 2 <= 2 * dev.sm_count && splits * 2 <= Kg) splits *= 2;
+    return splits;
+}
+
+template <int MODE, bool FUSED>
+cudaError_t set_attributes() {
     static std::once_flag attr_once[64];
     static cudaError_t attr_err[64];
     int device = 0;
     cudaGetDevice(&device);
     std::call_once(attr_once[device & 63], [&] {
-        cudaError_t e = cudaFuncSetAttribute(gemm_decode_kernel<MODE>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        attr_err[device & 63] = e;
+        attr_err[device & 63] = cudaFuncSetAttribute(gemm_decode_kernel<MODE, FUSED>,
+                                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     });
-    if (attr_err[device & 63] != cudaSuccess) return attr_err[device & 63];
+    return attr_err[device & 63];
+}
 
+template <int MODE, bool FUSED = false>
+cudaError_t launch_variant(const void *qa, const float *sa, const void *qw, const float *sw, void *y, int64_t M,
+                           int64_t N, int64_t K, const DeviceInfo &dev, cudaStream_t stream,
+                           FusedQuant fq = FusedQuant{nullptr, nullptr, nullptr}) {
+    if (cudaError_t e = set_attributes<MODE, FUSED>()) return e;
     CUtensorMap tmW, tmX;
     if (encode_tma_2d_u8(&tmW, qw, K, N, K, BK, kRows) != CUDA_SUCCESS) return cudaErrorInvalidValue;
     if (encode_tma_2d_u8(&tmX, qa, K, M, K, BK, kTok) != CUDA_SUCCESS) return cudaErrorInvalidValue;
 
     const int64_t nblocks = (N + kRows - 1) / kRows;
-    const int64_t Kg = (K + BK - 1) / BK;
-    // Split K over a cluster as far as all CTAs still fit on the GPU at once
-    // (two per SM), so that no CTA waits for a second wave.
-    int splits = 1;
-    while (splits < 8 && nblocks * splits * 2 <= 2 * dev.sm_count && splits * 2 <= Kg) splits *= 2;
+    const int splits = pick_splits(N, K, dev);
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(nblocks * splits));
@@ -393,9 +452,9 @@ cudaError_t launch_variant(const void *qa, const float *sa, const void *qw, cons
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, gemm_decode_kernel<MODE>, tmW, tmX, sa, sw,
+    return cudaLaunchKernelEx(&cfg, gemm_decode_kernel<MODE, FUSED>, tmW, tmX, sa, sw,
                               static_cast<__nv_bfloat16 *>(y), static_cast<int>(M), static_cast<int>(N),
-                              static_cast<int>(K), splits, dev.err);
+                              static_cast<int>(K), splits, dev.err, fq);
 }
 
 }  // namespace
@@ -406,6 +465,33 @@ cudaError_t launch_gemm_decode(const void *qa, const float *sa, const void *qw, 
     if (mode == kScaleTensor) return launch_variant<kScaleTensor>(qa, sa, qw, sw, y, M, N, K, dev, stream);
     if (mode == kScaleRowCol) return launch_variant<kScaleRowCol>(qa, sa, qw, sw, y, M, N, K, dev, stream);
     return launch_variant<kScaleBlock>(qa, sa, qw, sw, y, M, N, K, dev, stream);
+}
+
+bool decode_fused_fits(int64_t N, int64_t K, const DeviceInfo &dev) {
+    if (set_attributes<kScaleBlock, true>() != cudaSuccess) return false;
+    const int splits = pick_splits(N, K, dev);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(((N + kRows - 1) / kRows) * splits));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(splits);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, gemm_decode_kernel<kScaleBlock, true>, &cfg) != cudaSuccess)
+        return false;
+    return static_cast<int64_t>(clusters) >= (N + kRows - 1) / kRows;
+}
+
+cudaError_t launch_gemm_decode_fused(const void *x, void *qa, float *sa, const void *qw, const float *sw, void *y,
+                                     int64_t M, int64_t N, int64_t K, unsigned *ws, const DeviceInfo &dev,
+                                     cudaStream_t stream) {
+    const FusedQuant fq{static_cast<const uint16_t *>(x), static_cast<uint8_t *>(qa), ws};
+    return launch_variant<kScaleBlock, true>(qa, sa, qw, sw, y, M, N, K, dev, stream, fq);
 }
 
 }  // namespace fp8k

@@ -51,10 +51,26 @@ cudaError_t launch_gemm_prefill(const void *qa, const float *sa, const void *qw,
                                 int64_t M, int64_t N, int64_t K, int num_groups, const int32_t *offsets,
                                 ScaleMode mode, const DeviceInfo &dev, cudaStream_t stream);
 
+// The grouped block-scaled prefill GEMM with a row gather: row m of the
+// problem is row row_index[m] of qa [M_src][K] (scales sa [K/128][M_src]).
+cudaError_t launch_gemm_prefill_gather(const void *qa, const float *sa, const int32_t *row_index, int64_t M_src,
+                                       const void *qw, const float *sw, void *y, int64_t M, int64_t N, int64_t K,
+                                       int num_groups, const int32_t *offsets, const DeviceInfo &dev,
+                                       cudaStream_t stream);
+
 // Weight-streaming tcgen05 GEMM for M <= 16 (weights as the MMA's M side).
 cudaError_t launch_gemm_decode(const void *qa, const float *sa, const void *qw, const float *sw, void *y,
                                int64_t M, int64_t N, int64_t K, ScaleMode mode, const DeviceInfo &dev,
                                cudaStream_t stream);
+
+// The decode GEMM with the 1x128 activation quantization fused in (M <= 16,
+// block mode): every CTA quantizes a share of x into qa / sa, the grid meets
+// at a barrier kept in ws (two zeroed words), then the GEMM reads the codes.
+// Only valid when decode_fused_fits(): every CTA of the grid resident at once.
+bool decode_fused_fits(int64_t N, int64_t K, const DeviceInfo &dev);
+cudaError_t launch_gemm_decode_fused(const void *x, void *qa, float *sa, const void *qw, const float *sw, void *y,
+                                     int64_t M, int64_t N, int64_t K, unsigned *ws, const DeviceInfo &dev,
+                                     cudaStream_t stream);
 
 // One CTA whose waits never complete: the first gives up after the wait limit
 // and records FP8_ERR_TIMEOUT (site 901); the second returns at the abort flag.

@@ -63,23 +63,7 @@ __global__ void __launch_bounds__(kActThreads, 6) quant_act_group_kernel(const u
     grid_dep_wait();
 
     const int64_t g = static_cast<int64_t>(blockIdx.y) * kActGroups + (lane >> 2);
-    const bool ok = m < M && g < Kg;
-    const int64_t base = m * K + g * 128 + c * 8;
-    uint4 v[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        v[i] = make_uint4(0u, 0u, 0u, 0u);
-        if (ok) v[i] = ld_stream_v4(x + base + 32 * i);
-    }
-    float a = fmaxf(fmaxf(amax8(v[0]), amax8(v[1])), fmaxf(amax8(v[2]), amax8(v[3])));
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
-    if (ok) {
-        const float sc = block_scale(a);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) *reinterpret_cast<uint2 *>(q + base + 32 * i) = quant8(v[i], sc);
-        if (c == 0) s[g * M + m] = sc;
-    }
+    quant_group_by_quad(x, q, s, M, K, m, g, c, m < M && g < Kg, [](const uint16_t *p) { return ld_stream_v4(p); });
 }
 
 // --------------------------------------------------- 128 x 128 weight blocks --

@@ -133,6 +133,24 @@ def fp8_block_gemm(qa, sa, qw, sw, y, block_n: int = GROUP, block_k: int = GROUP
                                       _stream(stream)), "fp8_block_gemm")
 
 
+def fp8_block_gemm_gather(qa, sa, row_index, qw, sw, y, group_offsets, stream=None) -> None:
+    """Grouped GEMM over routed rows: row m reads row row_index[m] of qa [M_src, K]."""
+    M_src, K = qa.shape
+    M = row_index.shape[0]
+    N = y.shape[1]
+    G = qw.shape[0] if qw.dim() == 3 else 1
+    _need(sa, _cdiv(K, GROUP) * M_src, "sa")
+    _need(qw, G * N * K, "qw")
+    _need(sw, G * _cdiv(N, GROUP) * _cdiv(K, GROUP), "sw")
+    _need(y, M * N, "y")
+    _need(group_offsets, G + 1, "group_offsets")
+    args = _ptrs((qa, CODES, "qa"), (sa, torch.float32, "sa"), (row_index, torch.int32, "row_index"),
+                 (qw, CODES, "qw"), (sw, torch.float32, "sw"), (y, torch.bfloat16, "y"),
+                 (group_offsets, torch.int32, "group_offsets"))
+    _check(_lib.load().fp8_block_gemm_gather(args[0], args[1], args[2], M_src, args[3], args[4], args[5], M, N, K,
+                                             G, args[6], _stream(stream)), "fp8_block_gemm_gather")
+
+
 def fp8_tensor_gemm(qa, sa, qw, sw, y, stream=None) -> None:
     M, K = qa.shape
     N = y.shape[1]
@@ -156,6 +174,29 @@ def fp8_block_linear(x, qa, sa, qw, sw, y, stream=None) -> None:
     args = _ptrs((x, torch.bfloat16, "x"), (qa, CODES, "qa"), (sa, torch.float32, "sa"), (qw, CODES, "qw"),
                  (sw, torch.float32, "sw"), (y, torch.bfloat16, "y"))
     _check(_lib.load().fp8_block_linear(*args, M, N, K, _stream(stream)), "fp8_block_linear")
+
+
+FUSED_WORKSPACE_BYTES = 8
+
+
+def fused_workspace(device=None) -> torch.Tensor:
+    """A zeroed workspace for fp8_block_linear_fused (one per stream)."""
+    return torch.zeros(FUSED_WORKSPACE_BYTES // 4, dtype=torch.int32, device=device or "cuda")
+
+
+def fp8_block_linear_fused(x, qa, sa, qw, sw, y, workspace, stream=None) -> None:
+    M, K = x.shape
+    N = y.shape[1]
+    _need(qa, M * K, "qa")
+    _need(sa, _cdiv(K, GROUP) * M, "sa")
+    _need(qw, N * K, "qw")
+    _need(sw, _cdiv(N, GROUP) * _cdiv(K, GROUP), "sw")
+    _need(y, M * N, "y")
+    args = _ptrs((x, torch.bfloat16, "x"), (qa, CODES, "qa"), (sa, torch.float32, "sa"), (qw, CODES, "qw"),
+                 (sw, torch.float32, "sw"), (y, torch.bfloat16, "y"), (workspace, torch.int32, "workspace"))
+    ws_bytes = workspace.numel() * 4
+    _check(_lib.load().fp8_block_linear_fused(*args[:6], M, N, K, args[6], ws_bytes, _stream(stream)),
+           "fp8_block_linear_fused")
 
 
 def fp8_quant_rowwise(x, q, scales, stream=None) -> None:
@@ -296,6 +337,17 @@ def rowwise_gemm(qa, sa, qw, sw, stream=None) -> torch.Tensor:
     y = torch.empty((qa.shape[0], qw.shape[0]), dtype=torch.bfloat16, device=qa.device)
     fp8_rowwise_gemm(qa, sa, qw, sw, y, stream=stream)
     return y
+
+
+def block_linear_fused(x, qw, sw, workspace, stream=None):
+    """As block_linear, through fp8_block_linear_fused with the given workspace."""
+    M, K = x.shape
+    N = qw.shape[0]
+    qa = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    sa = torch.empty((K // GROUP, M), dtype=torch.float32, device=x.device)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    fp8_block_linear_fused(x, qa, sa, qw, sw, y, workspace, stream=stream)
+    return y, qa, sa
 
 
 def tensor_gemm(qa, sa, qw, sw, stream=None) -> torch.Tensor:

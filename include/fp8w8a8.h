@@ -52,8 +52,9 @@
  * let the next kernel launch before they complete (griddepcontrol.
  * launch_dependents). A dependent always waits for its predecessor to
  * complete before it reads that predecessor's outputs - with one exception:
- * the decode GEMM (fp8_block_gemm dense, fp8_tensor_gemm, fp8_rowwise_gemm
- * and fp8_block_linear, each with M <= 16) starts loading qw before that wait.
+ * the decode GEMM (fp8_block_gemm dense, fp8_tensor_gemm, fp8_rowwise_gemm,
+ * fp8_block_linear and fp8_block_linear_fused, each with M <= 16) starts
+ * loading qw before that wait.
  * So qw must not be written by a kernel that lets its dependents launch
  * early. Per entry point:
  *    fp8_quant_act_group     lets its dependent launch early (its q and s are
@@ -68,7 +69,9 @@
  *    prefill GEMM            does not;
  *    fp8_block_linear        its quantizer lets its own GEMM launch early (the
  *                            GEMM reads qa and sa after its wait); its GEMM is
- *                            the decode or prefill GEMM above.
+ *                            the decode or prefill GEMM above;
+ *    fp8_block_linear_fused  as the decode GEMM (one kernel), or as
+ *                            fp8_block_linear where it falls back to it.
  * Work that is not this library's (torch kernels, copies) never triggers
  * early, so a plain stream order with it is always safe.
  */
@@ -193,6 +196,34 @@ int fp8_block_gemm(const void *qa, const float *sa, const void *qw, const float 
                    int num_groups, const int32_t *group_offsets, void *stream);
 
 /*
+ * Grouped (mixture-of-experts) block-scaled GEMM that gathers its activation
+ * rows: row m of the problem is row row_index[m] of the token-order codes, so
+ * the routed (expert-sorted) activations are never materialised
+ * (Fp8MoEMethod of "[vLLM] FP8", section "Fp8Config: 온라인 vs 오프라인"; the
+ * routing itself is the caller's). Same formula as fp8_block_gemm, grouped:
+ *   Y[m,n] = bf16( sum_g Sa[g][r] Sw_e[n/128][g] sum_{k in g} dec(Qa[r,k]) dec(Qw_e[n,k]) ),
+ *   r = row_index[m], e the expert whose range holds m.
+ *
+ *   qa         [M_src][K] E4M3 and sa [K/128][M_src] FP32: the tokens'
+ *              codes and scales in token order (fp8_quant_act_group on X).
+ *   row_index  DEVICE int32 [M], 16-byte aligned: the source row of each
+ *              routed row. Values outside [0, M_src) read zero codes and are
+ *              recorded as FP8_ERR_ARG (site 107) in the device error word.
+ *   qw, sw     [num_groups][N][K] and [num_groups][ceil(N/128)][K/128].
+ *   y          [M][N] BF16, output, routed order.
+ *   group_offsets  DEVICE int32 [num_groups+1] over the M routed rows, as in
+ *              fp8_block_gemm (required here); rows outside all experts are
+ *              not written.
+ *   K a positive multiple of 128, N a positive multiple of 16, M >= 0,
+ *   M_src >= 1, num_groups in [1, FP8_MAX_GROUPS].
+ * The A tiles are loaded by row-gather TMA (four rows per instruction).
+ * Errors: NULL, SHAPE, ALIGN, UNSUPPORTED, ARG, DEVICE, CUDA.
+ */
+int fp8_block_gemm_gather(const void *qa, const float *sa, const int32_t *row_index, int64_t M_src,
+                          const void *qw, const float *sw, void *y_bf16, int64_t M, int64_t N, int64_t K,
+                          int num_groups, const int32_t *group_offsets, void *stream);
+
+/*
  * Per-tensor FP8 GEMM: Y[m,n] = bf16( sa * sw * sum_k dec(Qa[m,k]) dec(Qw[n,k]) ),
  * FP32 accumulation over all of K, one scale product applied at the end.
  *
@@ -302,6 +333,38 @@ int fp8_kv_cache_load(const void *key_cache, const void *value_cache, void *key_
  */
 int fp8_block_linear(const void *x_bf16, void *qa, float *sa, const void *qw, const float *sw,
                      void *y_bf16, int64_t M, int64_t N, int64_t K, void *stream);
+
+/* Bytes of caller workspace fp8_block_linear_fused needs. */
+#define FP8_FUSED_WORKSPACE_BYTES 8
+
+/*
+ * W8A8 linear layer with the activation quantization inside the GEMM kernel,
+ * for decode (M <= 16). fp8_block_linear runs the quantizer as a kernel of its
+ * own, and at decode sizes that kernel is a latency step in every layer's
+ * dependency chain - the quantize/dequantize overhead that "FP8 Quantization"
+ * (section E, item 4) names as what can eat FP8's gain. Here every CTA of the
+ * decode GEMM quantizes an equal share of X's 1x128 groups (each group
+ * exactly once), the CTAs meet at a bounded grid-wide barrier, and then the
+ * GEMM reads the codes. qa, sa and y are bit-identical to fp8_block_linear's.
+ *
+ *   x_bf16, qa, sa, qw, sw, y, M, N, K  as fp8_block_linear.
+ *   workspace        DEVICE memory, at least FP8_FUSED_WORKSPACE_BYTES bytes,
+ *                    4-byte aligned, caller-owned: the barrier's counters. It
+ *                    must be zeroed once before first use; each call leaves it
+ *                    ready for the next. Calls that may run at the same time
+ *                    (on different streams) need different workspaces. After a
+ *                    call that reports FP8_ERR_TIMEOUT it must be zeroed again.
+ *   workspace_bytes  its size in bytes.
+ * The barrier needs every CTA of the GEMM resident at once. When the shape
+ * does not allow that, or M > 16, the call runs fp8_block_linear's two
+ * kernels instead (same results; the workspace is not touched). A barrier
+ * wait longer than about one second gives up and records FP8_ERR_TIMEOUT
+ * (site 207) in the device error word.
+ * Errors: NULL, SHAPE, ALIGN, ARG (workspace too small), DEVICE, CUDA.
+ */
+int fp8_block_linear_fused(const void *x_bf16, void *qa, float *sa, const void *qw, const float *sw,
+                           void *y_bf16, int64_t M, int64_t N, int64_t K, void *workspace,
+                           int64_t workspace_bytes, void *stream);
 
 /* Static, NUL-terminated description of a status code. Never NULL. */
 const char *fp8_status_string(int status);

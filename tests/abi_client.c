@@ -93,6 +93,42 @@ int main(void)
     EXPECT(fp8_tensor_gemm(FAKE, FAKE_F, FAKE, FAKE_F, FAKE, 4, 256, ((int64_t)1 << 31) + 16, NULL), FP8_ERR_SHAPE);
     EXPECT(fp8_block_linear(FAKE, FAKE, FAKE_F, FAKE, FAKE_F, FAKE, 4, (int64_t)1 << 31, 256, NULL), FP8_ERR_SHAPE);
 
+    /* the grid limits of the group and block quantizers, exactly at and past the bound */
+    EXPECT(fp8_quant_act_group(FAKE, FAKE, FAKE_F, 4, FP8_ACT_GROUP_MAX_K + FP8_GROUP, FP8_GROUP, NULL),
+           FP8_ERR_SHAPE);
+    EXPECT(fp8_quant_act_group(FAKE, FAKE, FAKE_F, 0, FP8_ACT_GROUP_MAX_K, FP8_GROUP, NULL), FP8_OK);
+    EXPECT(fp8_quant_weight_block(FAKE, FAKE, FAKE_F, FP8_WEIGHT_BLOCK_MAX_N + 1, 256, FP8_GROUP, FP8_GROUP, NULL),
+           FP8_ERR_SHAPE);
+
+    /* row-wise quantization and GEMM */
+    EXPECT(fp8_quant_rowwise(FAKE, FAKE, FAKE_F, 4, 24, NULL), FP8_ERR_SHAPE);
+    EXPECT(fp8_quant_rowwise(FAKE, NULL, FAKE_F, 4, 32, NULL), FP8_ERR_NULL);
+    EXPECT(fp8_quant_rowwise(ODD8, FAKE, FAKE_F, 4, 32, NULL), FP8_ERR_ALIGN);
+    EXPECT(fp8_quant_rowwise(NULL, NULL, NULL, 0, 32, NULL), FP8_OK);
+    EXPECT(fp8_rowwise_gemm(FAKE, FAKE_F, FAKE, FAKE_F, FAKE, 4, 24, 256, NULL), FP8_ERR_SHAPE);
+    EXPECT(fp8_rowwise_gemm(FAKE, FAKE_F, FAKE, ODD2_F + 1, FAKE, 4, 256, 256, NULL), FP8_ERR_ALIGN); /* sw 16 B */
+    EXPECT(fp8_rowwise_gemm(FAKE, FAKE_F, FAKE, NULL, FAKE, 4, 256, 256, NULL), FP8_ERR_NULL);
+
+    /* FP8 KV cache */
+    EXPECT(fp8_kv_cache_store(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE_F, FAKE_F, 4, 24, 8, NULL), FP8_ERR_SHAPE);
+    EXPECT(fp8_kv_cache_store(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE_F, NULL, 4, 128, 8, NULL), FP8_ERR_NULL);
+    EXPECT(fp8_kv_cache_load(FAKE, FAKE, FAKE, FAKE, (const int64_t *)ODD2_I, FAKE_F, FAKE_F, 4, 128, 8, NULL),
+           FP8_ERR_ALIGN);
+    EXPECT(fp8_kv_cache_load(NULL, NULL, NULL, NULL, NULL, NULL, NULL, 0, 128, 8, NULL), FP8_OK);
+
+    /* the fused linear layer: its workspace is required and sized */
+    EXPECT(fp8_block_linear_fused(FAKE, FAKE, FAKE_F, FAKE, FAKE_F, FAKE, 4, 256, 256, NULL, 64, NULL),
+           FP8_ERR_NULL);
+    EXPECT(fp8_block_linear_fused(FAKE, FAKE, FAKE_F, FAKE, FAKE_F, FAKE, 4, 256, 256, FAKE,
+                                  FP8_FUSED_WORKSPACE_BYTES - 4, NULL),
+           FP8_ERR_ARG);
+    EXPECT(fp8_block_linear_fused(FAKE, FAKE, FAKE_F, FAKE, FAKE_F, FAKE, 4, 256, 256, ODD2_F,
+                                  FP8_FUSED_WORKSPACE_BYTES, NULL),
+           FP8_ERR_ALIGN);
+    EXPECT(fp8_block_linear_fused(FAKE, FAKE, FAKE_F, FAKE, FAKE_F, FAKE, 4, 256, 200, FAKE,
+                                  FP8_FUSED_WORKSPACE_BYTES, NULL),
+           FP8_ERR_SHAPE);
+
     /* the conversion self-test: n a multiple of 8, no pattern past 0xFFFFFFFF */
     EXPECT(fp8_selftest_encode_f32(0, 12, FAKE, NULL), FP8_ERR_SHAPE);
     EXPECT(fp8_selftest_encode_f32(0, -8, FAKE, NULL), FP8_ERR_SHAPE);

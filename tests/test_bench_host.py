@@ -85,7 +85,7 @@ def test_committed_traffic_file_is_well_formed():
 
 
 def test_reference_arm_line(monkeypatch):
-    monkeypatch.setattr(bench, "oracle_decode_sample", lambda budget: (0.25, "a sample", 0.1))
+    monkeypatch.setattr(bench, "oracle_decode_sample", lambda threads=None, ms=None, cols=None: (0.25, "a sample", 0.1))
     args = types.SimpleNamespace(gpus=1, steps=2, warmup=3)
     out = io.StringIO()
     with redirect_stdout(out):
@@ -101,7 +101,21 @@ def test_reference_arm_line(monkeypatch):
     assert host["logical_cpus"] == os.cpu_count() and host["machine"] and isinstance(host["model"], str)
 
 
-def test_oracle_sample_runs_on_a_tiny_budget():
-    gbps, desc, seconds = bench.oracle_decode_sample(0.001)
+def test_oracle_sample_runs_on_a_small_slice():
+    gbps, desc, seconds = bench.oracle_decode_sample(2, ms=[1, 4], cols=256)
     assert gbps > 0 and seconds > 0
-    assert "[128, 128, 128, 128]" in desc  # the smallest sample: one 128-column block per projection
+    assert "[256, 256, 256, 256]" in desc and "2 host thread(s)" in desc
+
+
+def test_oracle_sample_threads_cover_every_column(monkeypatch):
+    """The column split over threads covers each projection's columns once."""
+    import oracle
+    seen = []
+    real = oracle.gemm_block
+
+    def spy(qa, sa, qw, sw, **kw):
+        seen.append(qw.shape[0])
+        return real(qa, sa, qw, sw, **kw)
+    monkeypatch.setattr(oracle, "gemm_block", spy)
+    bench.oracle_decode_sample(3, ms=[1], cols=640)
+    assert sum(seen) == 4 * 640 and all(n % 128 == 0 for n in seen)
