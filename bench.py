@@ -271,21 +271,21 @@ def decode_calls():
 def run_decode_section(torch, ops, dev, steps, warmup, peaks, sync_ranks):
     layers, acts = build_decode(torch, ops, dev)
     calls = decode_calls()
-    ws = ops.fused_workspace(dev)  # the grid barrier's words, one per stream
 
     def step(marks):
         for (M, layer, i) in calls:
             N, K = SHAPES[i]
             x, qa, sa, ys = acts[(M, N, K)]
             qw, sw = layers[layer][i]
-            ops.fp8_block_linear_fused(x, qa, sa, qw, sw, ys[layer], ws)
+            ops.fp8_block_linear(x, qa, sa, qw, sw, ys[layer])
 
     def step_two_kernels(marks):
         for (M, layer, i) in calls:
             N, K = SHAPES[i]
             x, qa, sa, ys = acts[(M, N, K)]
             qw, sw = layers[layer][i]
-            ops.fp8_block_linear(x, qa, sa, qw, sw, ys[layer])
+            ops.fp8_quant_act_group(x, qa, sa)
+            ops.fp8_block_gemm(qa, sa, qw, sw, ys[layer])
 
     step_bytes = sum(linear_bytes(M, *SHAPES[i]) for M, _, i in calls)
     gemm_total_bytes = sum(gemm_bytes(M, *SHAPES[i]) for M, _, i in calls)
@@ -328,7 +328,8 @@ def run_decode_section(torch, ops, dev, steps, warmup, peaks, sync_ranks):
     out = {"value": value, "ms_per_step": ms / steps, "roofline": roof, "per_shape": per_shape,
            "launches_per_step": len(calls), "window": window, "step_bytes": step_bytes,
            "two_kernel_path": {"value": step_bytes * steps / (ms2 * 1e-3) / 1e9, "ms_per_step": ms2 / steps,
-                               "note": "the same step through fp8_block_linear (quantizer kernel + GEMM kernel)"}}
+                               "note": "the same step as fp8_quant_act_group + fp8_block_gemm (a quantizer kernel "
+                                       "and a GEMM kernel per call, chained by programmatic dependent launch)"}}
 
     # End to end through the C entry point, as a C caller drives it: the step's
     # 96 activation inputs sit in one pinned host slab and its 96 outputs
@@ -357,15 +358,14 @@ def run_decode_section(torch, ops, dev, steps, warmup, peaks, sync_ranks):
     d2h = y_host.numel() * 2
     stream = torch.cuda.current_stream()
     handle = stream.cuda_stream
-    linear = lib.fp8_block_linear_fused
-    ws_ptr, ws_bytes = ws.data_ptr(), ws.numel() * 4
+    linear = lib.fp8_block_linear
 
     def e2e_step():
         x_dev.copy_(x_host, non_blocking=True)
         for a in args:
-            st = linear(*a, ws_ptr, ws_bytes, handle)
+            st = linear(*a, handle)
             if st:
-                raise RuntimeError(f"fp8_block_linear_fused: status {st}")
+                raise RuntimeError(f"fp8_block_linear: status {st}")
         y_host.copy_(y_dev, non_blocking=True)
 
     e2e_steps = max(1, min(steps, 20))
@@ -373,7 +373,7 @@ def run_decode_section(torch, ops, dev, steps, warmup, peaks, sync_ranks):
     out["e2e"] = {"value": step_bytes * e2e_steps / (ms_e2e * 1e-3) / 1e9, "unit": "GB/s",
                   "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                   "ms_per_step": ms_e2e / e2e_steps,
-                  "note": "eager C-ABI calls of fp8_block_linear_fused (no graph); per step one pinned "
+                  "note": "eager C-ABI calls of fp8_block_linear (no graph); per step one pinned "
                           "host->device copy of the 96 inputs and one device->host copy of the 96 outputs, on the "
                           "compute stream"}
     del layers, acts
@@ -473,20 +473,19 @@ def run_tensor_section(torch, ops, dev, steps, warmup, peaks):
 
 def run_moe_section(torch, ops, dev, steps, warmup, peaks):
     """Mixture-of-experts layer: 8 experts [2048, 7168], 4096 tokens routed
-    top-2 (8192 rows). Timed: activation quantization of the tokens in token
-    order + the grouped GEMM that gathers each routed row (row-gather TMA);
-    also the GEMM alone, and the older route through a permuted copy."""
+    top-2 (8192 rows). Timed after a 256 MB L2 flush: the activation
+    quantization of the routed rows, read through the routing index from the
+    token-order X (no permuted copy), then the grouped GEMM."""
     tokens, E, N, K = 4096, 8, 2048, 7168
     token_of_row, offsets = synth.route_top2(tokens, E, seed=0)
     x = synth.device_normal_bf16(tokens, K, 0, "bench/moe/X", device=dev)
     ri = torch.from_numpy(token_of_row.astype(np.int32)).to(dev)
-    xp = x.index_select(0, torch.from_numpy(token_of_row).to(dev))  # the permuted copy (older route, untimed)
     qw = torch.empty((E, N, K), dtype=torch.uint8, device=dev)
     sw = torch.empty((E, N // 128, K // 128), dtype=torch.float32, device=dev)
     for e in range(E):
         w = synth.device_normal_bf16(N, K, 0, f"bench/moe/W{e}", sigma=0.02, device=dev)
         ops.fp8_quant_weight_block(w, qw[e], sw[e])
-    M = xp.shape[0]
+    M = ri.shape[0]
     qa = torch.empty((M, K), dtype=torch.uint8, device=dev)
     sa = torch.empty((K // 128, M), dtype=torch.float32, device=dev)
     y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
@@ -495,47 +494,32 @@ def run_moe_section(torch, ops, dev, steps, warmup, peaks):
 
     def step(marks):
         flush.zero_()
-        ops.fp8_quant_act_group(xp, qa, sa)
         if marks:
             marks[0][0].record()
+        ops.fp8_quant_act_group_gather(x, ri, qa, sa)
+        if marks:
+            marks[1][0].record()
         ops.fp8_block_gemm(qa, sa, qw, sw, y, num_groups=E, group_offsets=off)
         if marks:
             marks[0][1].record()
+            marks[1][1].record()
 
-    timed = Timed(torch, step, n_marks=1)
+    timed = Timed(torch, step, n_marks=2)
     time_steps(torch, timed.replay, steps, warmup)
     out = {"counts": np.diff(offsets).tolist()}
     fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
     fl = 2.0 * M * N * K
     if timed.ext:
-        t = timed.mark_ms()[0] * 1e-3
-        out["permuted_copy"] = {"gemm_us": t * 1e6, "TFLOPS": fl / t / 1e12, "frac_fp8_peak": fl / t / 1e12 / fp8_peak}
-    qt = torch.empty((tokens, K), dtype=torch.uint8, device=dev)
-    st = torch.empty((K // 128, tokens), dtype=torch.float32, device=dev)
-
-    def step_gather(marks):
-        flush.zero_()
-        if marks:
-            marks[0][0].record()
-        ops.fp8_quant_act_group(x, qt, st)
-        if marks:
-            marks[1][0].record()
-        ops.fp8_block_gemm_gather(qt, st, ri, qw, sw, y, off)
-        if marks:
-            marks[0][1].record()
-            marks[1][1].record()
-    tg = Timed(torch, step_gather, n_marks=2)
-    ms, _ = time_steps(torch, tg.replay, steps, warmup)
-    if tg.ext:
-        t_all, t_gemm = (v * 1e-3 for v in tg.mark_ms())
+        t_all, t_gemm = (v * 1e-3 for v in timed.mark_ms())
         out.update({"us": t_gemm * 1e6, "TFLOPS": fl / t_gemm / 1e12, "frac_fp8_peak": fl / t_gemm / 1e12 / fp8_peak,
                     "layer_us": t_all * 1e6, "layer_TFLOPS": fl / t_all / 1e12,
+                    "quant_gather_GBps": (2 * M * K + M * K + 4 * M * K // 128) / (t_all - t_gemm) / 1e9,
                     "roofline": {"bound": "tensor", "achieved": fl / t_gemm / 1e12, "peak": fp8_peak,
                                  "unit": "TFLOP/s", "frac": fl / t_gemm / 1e12 / fp8_peak,
                                  "peak_source": f"bf16_tflops of {peaks['source']} x {FP8_OVER_BF16}"},
-                    "note": "TFLOPS of the row-gather grouped GEMM; layer_* = token-order activation "
-                            "quantization + that GEMM, after a 256 MB L2 flush"})
-    del x, xp
+                    "note": "TFLOPS of the grouped GEMM; layer_* = routed-row activation quantization from "
+                            "token-order X + the GEMM"})
+    del x
     return out
 
 
@@ -783,7 +767,7 @@ def reference_arm(args):
 
 def run_case(spec: str, launches: int):
     """One kernel on one shape, for profiling: KIND:M:N:K with KIND in
-    decode|prefill|linear|fused|tensor|moe|act|weight|ptensor. Prints per-launch times."""
+    decode|prefill|linear|tensor|moe|act|weight|ptensor. Prints per-launch times."""
     import torch
 
     import __graft_entry__
@@ -805,13 +789,6 @@ def run_case(spec: str, launches: int):
         qw, sw = ops.quant_weight_block(synth.device_normal_bf16(N, K, 0, "case/W", sigma=0.02, device=dev))
         y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
         fn = lambda: ops.fp8_block_linear(x, qa, sa, qw, sw, y)  # noqa: E731
-    elif kind == "fused":
-        qa = torch.empty((M, K), dtype=torch.uint8, device=dev)
-        sa = torch.empty((K // 128, M), dtype=torch.float32, device=dev)
-        qw, sw = ops.quant_weight_block(synth.device_normal_bf16(N, K, 0, "case/W", sigma=0.02, device=dev))
-        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-        ws = ops.fused_workspace(dev)
-        fn = lambda: ops.fp8_block_linear_fused(x, qa, sa, qw, sw, y, ws)  # noqa: E731
     elif kind == "tensor":
         qa, sa = ops.quant_per_tensor(x)
         qw, sw = ops.quant_per_tensor(synth.device_normal_bf16(N, K, 0, "case/W", sigma=0.02, device=dev))
@@ -947,6 +924,7 @@ def main():
                          f"({sum(N * K for N, K in SHAPES) * LAYERS / 1e9:.2f} GB) stream once per M per step",
                    "graph": "each step is one CUDA graph replay"},
         "roofline": dec["roofline"], "cpu_baseline": cpu, "e2e": dec["e2e"],
+        "two_kernel_path": dec["two_kernel_path"],
         "gpu_launches": dec["launches_per_step"] * args.steps, "clocks": clocks,
         "decode_per_shape": dec["per_shape"], "sections": sections,
         "device_error": {"code": code, "site": site}, "peaks": peaks,

@@ -9,18 +9,15 @@ from .ops import (  # noqa: F401
     Fp8Error,
     block_gemm,
     block_linear,
-    block_linear_fused,
-    fused_workspace,
     fp8_block_gemm,
-    fp8_block_gemm_gather,
     fp8_block_linear,
-    fp8_block_linear_fused,
     fp8_device_error,
     fp8_kv_cache_load,
     fp8_kv_cache_store,
     fp8_selftest_bounded_wait,
     fp8_selftest_encode_f32,
     fp8_quant_act_group,
+    fp8_quant_act_group_gather,
     fp8_quant_per_tensor,
     fp8_quant_rowwise,
     fp8_quant_weight_block,

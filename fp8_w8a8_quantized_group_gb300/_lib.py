@@ -22,13 +22,12 @@ I32 = ctypes.c_int
 
 SIGNATURES = {
     "fp8_quant_act_group": ([P, P, P, I64, I64, I32, P], I32),
+    "fp8_quant_act_group_gather": ([P, P, P, P, I64, I64, I64, I32, P], I32),
     "fp8_quant_weight_block": ([P, P, P, I64, I64, I32, I32, P], I32),
     "fp8_quant_per_tensor": ([P, P, P, I64, I64, I32, P], I32),
     "fp8_block_gemm": ([P, P, P, P, P, I64, I64, I64, I32, I32, I32, I32, P, P], I32),
     "fp8_tensor_gemm": ([P, P, P, P, P, I64, I64, I64, P], I32),
-    "fp8_block_gemm_gather": ([P, P, P, I64, P, P, P, I64, I64, I64, I32, P, P], I32),
     "fp8_block_linear": ([P, P, P, P, P, P, I64, I64, I64, P], I32),
-    "fp8_block_linear_fused": ([P, P, P, P, P, P, I64, I64, I64, P, I64, P], I32),
     "fp8_quant_rowwise": ([P, P, P, I64, I64, P], I32),
     "fp8_rowwise_gemm": ([P, P, P, P, P, I64, I64, I64, P], I32),
     "fp8_kv_cache_store": ([P, P, P, P, P, P, P, I64, I64, I64, P], I32),

@@ -103,6 +103,23 @@ int fp8_quant_act_group(const void *x_bf16, void *q_e4m3, float *scales, int64_t
                                                         static_cast<cudaStream_t>(stream)));
 }
 
+int fp8_quant_act_group_gather(const void *x_bf16, const int32_t *row_index, void *q_e4m3, float *scales, int64_t M,
+                               int64_t M_src, int64_t K, int group_k, void *stream) {
+    if (M < 0 || K < 0 || M_src < 0) return FP8_ERR_SHAPE;
+    if (group_k != FP8_GROUP) return FP8_ERR_UNSUPPORTED;
+    if (K == 0 || K % FP8_GROUP != 0 || M > INT_MAX || K > FP8_ACT_GROUP_MAX_K || M_src > INT_MAX)
+        return FP8_ERR_SHAPE;
+    if (M == 0) return FP8_OK;
+    if (M_src == 0) return FP8_ERR_SHAPE;
+    if (!x_bf16 || !row_index || !q_e4m3 || !scales) return FP8_ERR_NULL;
+    if (misaligned(x_bf16, 16) || misaligned(q_e4m3, 16) || misaligned(scales, 4) || misaligned(row_index, 4))
+        return FP8_ERR_ALIGN;
+    const fp8k::DeviceInfo *dev = nullptr;
+    if (int st = fp8k::current_device(&dev)) return st;
+    return fp8k::to_status(fp8k::launch_quant_act_group(x_bf16, q_e4m3, scales, M, K, *dev,
+                                                        static_cast<cudaStream_t>(stream), row_index, M_src));
+}
+
 int fp8_quant_weight_block(const void *w_bf16, void *q_e4m3, float *scales, int64_t N, int64_t K, int block_n,
                            int block_k, void *stream) {
     if (N < 0 || K < 0) return FP8_ERR_SHAPE;
@@ -156,27 +173,6 @@ int fp8_block_gemm(const void *qa, const float *sa, const void *qw, const float 
                                                      fp8k::kScaleBlock, *dev, s));
 }
 
-int fp8_block_gemm_gather(const void *qa, const float *sa, const int32_t *row_index, int64_t M_src, const void *qw,
-                          const float *sw, void *y_bf16, int64_t M, int64_t N, int64_t K, int num_groups,
-                          const int32_t *group_offsets, void *stream) {
-    if (M < 0 || N < 0 || K < 0 || M_src < 0) return FP8_ERR_SHAPE;
-    if (num_groups < 1 || group_offsets == nullptr) return FP8_ERR_ARG;
-    if (num_groups > FP8_MAX_GROUPS) return FP8_ERR_UNSUPPORTED;
-    if (K == 0 || K % FP8_GROUP != 0 || N == 0 || N % 16 != 0 || M_src == 0) return FP8_ERR_SHAPE;
-    if (M > INT_MAX || M_src > INT_MAX || K > INT_MAX || N * static_cast<int64_t>(num_groups) > INT_MAX)
-        return FP8_ERR_SHAPE;
-    if (M == 0) return FP8_OK;
-    if (!qa || !sa || !row_index || !qw || !sw || !y_bf16) return FP8_ERR_NULL;
-    if (misaligned(qa, 16) || misaligned(qw, 16) || misaligned(y_bf16, 16) || misaligned(sa, 4) ||
-        misaligned(sw, 4) || misaligned(group_offsets, 4) || misaligned(row_index, 16))
-        return FP8_ERR_ALIGN;
-    const fp8k::DeviceInfo *dev = nullptr;
-    if (int st = fp8k::current_device(&dev)) return st;
-    return fp8k::to_status(fp8k::launch_gemm_prefill_gather(qa, sa, row_index, M_src, qw, sw, y_bf16, M, N, K,
-                                                            num_groups, group_offsets, *dev,
-                                                            static_cast<cudaStream_t>(stream)));
-}
-
 int fp8_tensor_gemm(const void *qa, const float *sa, const void *qw, const float *sw, void *y_bf16, int64_t M,
                     int64_t N, int64_t K, void *stream) {
     if (M < 0 || N < 0 || K < 0) return FP8_ERR_SHAPE;
@@ -199,7 +195,7 @@ int fp8_block_linear(const void *x_bf16, void *qa, float *sa, const void *qw, co
                      int64_t M, int64_t N, int64_t K, void *stream) {
     if (M < 0 || N < 0 || K < 0) return FP8_ERR_SHAPE;
     if (K == 0 || K % FP8_GROUP != 0 || N == 0 || N % 16 != 0) return FP8_ERR_SHAPE;
-    if (M > INT_MAX || N > INT_MAX || K > INT_MAX) return FP8_ERR_SHAPE;
+    if (M > INT_MAX || N > INT_MAX || K > FP8_ACT_GROUP_MAX_K) return FP8_ERR_SHAPE;
     if (M == 0) return FP8_OK;
     if (!x_bf16 || !qa || !sa || !qw || !sw || !y_bf16) return FP8_ERR_NULL;
     if (misaligned(x_bf16, 16) || misaligned(qa, 16) || misaligned(qw, 16) || misaligned(y_bf16, 16) ||
@@ -208,6 +204,8 @@ int fp8_block_linear(const void *x_bf16, void *qa, float *sa, const void *qw, co
     const fp8k::DeviceInfo *dev = nullptr;
     if (int st = fp8k::current_device(&dev)) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (M <= 16)
+        return fp8k::to_status(fp8k::launch_gemm_decode_fused(x_bf16, qa, sa, qw, sw, y_bf16, M, N, K, *dev, s));
     cudaError_t e = fp8k::launch_quant_act_group(x_bf16, qa, sa, M, K, *dev, s);
     if (e != cudaSuccess) return FP8_ERR_CUDA;
     if (M <= 16) return fp8k::to_status(fp8k::launch_gemm_decode(qa, sa, qw, sw, y_bf16, M, N, K, fp8k::kScaleBlock, *dev, s));
@@ -284,33 +282,6 @@ int fp8_kv_cache_load(const void *key_cache, const void *value_cache, void *key_
     return fp8k::to_status(fp8k::launch_kv_load(key_cache, value_cache, key_bf16, value_bf16, slot_mapping, k_scale,
                                                 v_scale, num_tokens, token_elems, num_slots, *dev,
                                                 static_cast<cudaStream_t>(stream)));
-}
-
-int fp8_block_linear_fused(const void *x_bf16, void *qa, float *sa, const void *qw, const float *sw, void *y_bf16,
-                           int64_t M, int64_t N, int64_t K, void *workspace, int64_t workspace_bytes,
-                           void *stream) {
-    if (M < 0 || N < 0 || K < 0 || workspace_bytes < 0) return FP8_ERR_SHAPE;
-    if (K == 0 || K % FP8_GROUP != 0 || N == 0 || N % 16 != 0) return FP8_ERR_SHAPE;
-    if (M > INT_MAX || N > INT_MAX || K > FP8_ACT_GROUP_MAX_K) return FP8_ERR_SHAPE;
-    if (M == 0) return FP8_OK;
-    if (!x_bf16 || !qa || !sa || !qw || !sw || !y_bf16 || !workspace) return FP8_ERR_NULL;
-    if (workspace_bytes < FP8_FUSED_WORKSPACE_BYTES) return FP8_ERR_ARG;
-    if (misaligned(x_bf16, 16) || misaligned(qa, 16) || misaligned(qw, 16) || misaligned(y_bf16, 16) ||
-        misaligned(sa, 4) || misaligned(sw, 4) || misaligned(workspace, 4))
-        return FP8_ERR_ALIGN;
-    const fp8k::DeviceInfo *dev = nullptr;
-    if (int st = fp8k::current_device(&dev)) return st;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (M <= 16 && fp8k::decode_fused_fits(N, K, *dev))
-        return fp8k::to_status(fp8k::launch_gemm_decode_fused(x_bf16, qa, sa, qw, sw, y_bf16, M, N, K,
-                                                              static_cast<unsigned *>(workspace), *dev, s));
-    // Otherwise the two launches of fp8_block_linear (the workspace is not used).
-    cudaError_t e = fp8k::launch_quant_act_group(x_bf16, qa, sa, M, K, *dev, s);
-    if (e != cudaSuccess) return FP8_ERR_CUDA;
-    if (M <= 16)
-        return fp8k::to_status(fp8k::launch_gemm_decode(qa, sa, qw, sw, y_bf16, M, N, K, fp8k::kScaleBlock, *dev, s));
-    return fp8k::to_status(
-        fp8k::launch_gemm_prefill(qa, sa, qw, sw, y_bf16, M, N, K, 1, nullptr, fp8k::kScaleBlock, *dev, s));
 }
 
 const char *fp8_status_string(int status) {

@@ -108,22 +108,23 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
     return r;
 }
 
-// One 1 x 128 activation group (row m, group g of x [M][K]) quantized by a
-// lane quad: lane c (0..3) of the quad holds the 16-byte chunks c, c+4, c+8,
-// c+12 of the group's 256 bytes, the quad's amax is reduced with two
-// shuffles, and each lane stores its 4 x 8 codes; lane 0 of the quad stores
-// the scale at s[g * M + m]. Every lane of the warp must call it (ok = false
-// where the group does not exist, which loads, stores and contributes nothing).
-// `ld` loads 16 bytes of x.
+// One 1 x 128 activation group quantized by a lane quad: group g of row
+// src_row of x [.][K] into row m of q [M][K] and s [K/128][M]. Lane c (0..3) of
+// the quad holds the 16-byte chunks c, c+4, c+8, c+12 of the group's 256
+// bytes, the quad's amax is reduced with two shuffles, and each lane stores
+// its 4 x 8 codes; lane 0 of the quad stores the scale at s[g * M + m]. Every
+// lane of the warp must call it (ok = false where the group does not exist,
+// which loads, stores and contributes nothing). `ld` loads 16 bytes of x.
 template <typename Load>
 __device__ __forceinline__ void quant_group_by_quad(const uint16_t *x, uint8_t *q, float *s, int64_t M, int64_t K,
-                                                    int64_t m, int64_t g, int c, bool ok, Load ld) {
+                                                    int64_t m, int64_t src_row, int64_t g, int c, bool ok, Load ld) {
     const int64_t base = m * K + g * 128 + c * 8;
+    const int64_t src = src_row * K + g * 128 + c * 8;
     uint4 v[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         v[i] = make_uint4(0u, 0u, 0u, 0u);
-        if (ok) v[i] = ld(x + base + 32 * i);
+        if (ok) v[i] = ld(x + src + 32 * i);
     }
     float a = fmaxf(fmaxf(amax8(v[0]), amax8(v[1])), fmaxf(amax8(v[2]), amax8(v[3])));
     a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
@@ -251,19 +252,6 @@ __device__ __forceinline__ void tma_load_2d_hint(void *dst, const CUtensorMap *m
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
         " [%0], [%1, {%2, %3}], [%4], %5;"
         ::"r"(smem_u32(dst)), "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
-        : "memory");
-}
-
-// Row gather: four rows y0..y3 of a 2-D tensor map whose box is one row high
-// (box_inner x 1), columns from x, into four consecutive box rows at dst
-// (swizzled like a tile load at the same shared-memory addresses). A row at
-// or beyond the map's extent reads the fill value (zeros).
-__device__ __forceinline__ void tma_gather4(void *dst, const CUtensorMap *map, uint64_t *bar, int32_t x, int32_t y0,
-                                            int32_t y1, int32_t y2, int32_t y3) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
-        ::"r"(smem_u32(dst)), "l"(map), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(bar))
         : "memory");
 }
 
@@ -509,59 +497,6 @@ __device__ __forceinline__ uint32_t map_shared_rank(uint32_t saddr, uint32_t ran
     uint32_t r;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
     return r;
-}
-
-// ------------------------------------------------------- grid-wide sync --
-
-__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-// FP32 load through L2 only (no L1 or read-only-path caching): for data that
-// other CTAs of the running grid write.
-__device__ __forceinline__ float ld_cg_f32(const float *p) {
-    float v;
-    asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
-    return v;
-}
-
-// Make generic-proxy global writes (visible to this thread) visible to its
-// subsequent async-proxy reads (TMA).
-__device__ __forceinline__ void fence_proxy_async_global() {
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
-// One arrival of a CTA at a grid-wide barrier kept in two words of global
-// memory: ws[0] counts the arrivals of the current round, ws[1] the completed
-// rounds. The last of the n arrivals resets ws[0] to zero and advances ws[1];
-// the others wait for ws[1] to change. The words must start at zero (a reset
-// round leaves them so), and every CTA of the grid must be resident at once.
-// The caller makes its CTA's writes visible (a CTA barrier before this call)
-// and orders its later reads after it (another CTA barrier after). A wait
-// longer than kWaitLimitNs records FP8_ERR_TIMEOUT with `site`, raises *abort
-// and returns false; the words are then left mid-round.
-__device__ __forceinline__ bool grid_barrier(unsigned *ws, unsigned n, volatile int *abort, unsigned *err,
-                                             unsigned site) {
-    const unsigned round = ld_acquire_gpu(ws + 1);
-    __threadfence();
-    if (atomicAdd(ws, 1u) == n - 1u) {
-        atomicExch(ws, 0u);
-        __threadfence();
-        atomicAdd(ws + 1, 1u);
-        return true;
-    }
-    const uint64_t t0 = global_ns();
-    while (ld_acquire_gpu(ws + 1) == round) {
-        if (global_ns() - t0 > kWaitLimitNs) {
-            record_error(err, kErrTimeout, site);
-            *abort = 1;
-            return false;
-        }
-    }
-    __threadfence();
-    return true;
 }
 
 // ------------------------------------------------------------------- BF16 --

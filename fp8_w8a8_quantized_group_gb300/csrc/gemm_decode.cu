@@ -29,6 +29,19 @@
 //    early); the activation codes and scales are read, and every global
 //    write is made, after griddepcontrol.wait.
 //
+// Fused variant (fp8_block_linear, M <= 16): the 1x128 activation
+// quantization runs inside this kernel, in the operand pipeline. Two warps
+// take each stage's K block of X (BF16, at most 16 rows x 128), quantize it
+// (the same per-group scale and codes as the stand-alone quantizer) and write
+// the codes straight into the stage's shared-memory operand tile in the
+// swizzled layout the MMA reads, and the scales into a small ring the
+// epilogue reads; no code makes a round trip through global memory and no CTA
+// waits for another. Every CTA quantizes the K range it multiplies, so the
+// work is repeated once per 128-row block of weights - cheap here, since it
+// reads X from L2 and uses issue slots the weight stream leaves idle. The CTAs
+// of the first row block also write the codes and scales to qa and sa, so
+// each group is written exactly once.
+//
 // Block mode applies Sw[n/128][kb] * Sa[kb][m] per K block; per-tensor mode
 // accumulates all of the CTA's K range in TMEM and applies sa * sw once;
 // row/column mode does the same with sa[m] * sw[n] (per-token activation and
@@ -53,19 +66,23 @@ constexpr int kL2Warm = 12;     // weight tiles loaded or warmed in L2 before th
 constexpr int kScaleKb = 8;     // K blocks of activation/weight scales staged at a time per epilogue warp
 constexpr int kScaleBytes = 4 * 4 * (kScaleKb * kTok + kScaleKb);
 constexpr int kRecvBytes = kRows * kTok * 4;  // split-K partials addressed to this CTA
+constexpr int kXsRing = 8;     // fused: activation-scale slots, a ring over K blocks (>= kStages + 2)
+constexpr int kQuantBatch = 4; // fused: K blocks of X the quantizer warps load at once
+constexpr int kXsBytes = kXsRing * kTok * 4;
 constexpr int kSmemBytes =
-    1024 + kStages * (kWBytes + kXBytes) + kRecvBytes + 8 * (2 * kStages + 6) + 16 + kScaleBytes;
+    1024 + kStages * (kWBytes + kXBytes) + kRecvBytes + 8 * (3 * kStages + 5) + 16 + kScaleBytes + kXsBytes;
+static_assert(kXsRing >= kStages + 2, "a scale slot must outlive the K blocks the MMA runs ahead of the epilogue");
 
 enum : unsigned { kSiteProdEmpty = 201, kSiteMmaTmem = 202, kSiteMmaFull = 203, kSiteEpiFull = 204,
-                  kSiteDrain = 205, kSiteReduce = 206, kSiteGridSync = 207, kSiteQuantReady = 208 };
+                  kSiteDrain = 205, kSiteReduce = 206, kSiteQuantEmpty = 207 };
 
-// Optional fused activation quantization (block mode only): x is the BF16
-// input [M][K], the activation codes go to the tensor `tmX` maps (qa_out) and
-// the scales to sa, and ws is the grid barrier's two words.
+// Fused activation quantization (block mode only): x is the BF16 input
+// [M][K]; the CTAs of the first row block write the codes to qa_out and the
+// scales to sa_out ([K/128][M]).
 struct FusedQuant {
     const uint16_t *x;
     uint8_t *qa_out;
-    unsigned *ws;
+    float *sa_out;
 };
 
 template <int MODE, bool FUSED>
@@ -86,10 +103,12 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint64_t *tfull = empty + kStages;
     uint64_t *tempty = tfull + 2;
     uint64_t *rbar = tempty + 2;  // completes when all kRecvBytes have arrived
-    uint64_t *qready = rbar + 1;  // fused: every CTA's activation codes are in memory
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(qready + 1);
+    uint64_t *xfull = rbar + 1;   // fused: the stage's activation codes are written
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(xfull + kStages);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    volatile int *quant_go = reinterpret_cast<volatile int *>(tmem_slot + 2);  // fused: quantizer's shared decision
     float *scale_smem = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(tmem_slot) + 16);
+    float *xs_ring = scale_smem + kScaleBytes / 4;  // fused: [kXsRing][kTok] activation scales
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nb = blockIdx.x / splits;
@@ -100,10 +119,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int kb1 = static_cast<int>((static_cast<int64_t>(split + 1) * Kg) / splits);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+        // fused: the weights of a stage land on full[s], its activation codes
+        // (written by the quantizer warps) are announced on xfull[s].
+        for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); mbar_init(&xfull[s], 1); }
         for (int b = 0; b < 2; ++b) { mbar_init(&tfull[b], 1); mbar_init(&tempty[b], 128); }
         mbar_init(rbar, 1);
-        mbar_init(qready, 1);
         *abort_flag = 0;
         fence_barrier_init();
         if (splits > 1) mbar_arrive_expect_tx(rbar, kRecvBytes);
@@ -135,32 +155,24 @@ __global__ void __launch_bounds__(kThreads, 2)
             const uint64_t stream_once = policy_evict_first();
             const int nkb = kb1 - kb0;
             const int pre = nkb < kStages ? nkb : kStages;
+            constexpr uint32_t kStageTx = FUSED ? kWBytes : kWBytes + kXBytes;  // fused: X is not loaded by TMA
             for (int i = 0; i < pre; ++i) {
-                mbar_arrive_expect_tx(&full[i], kWBytes + kXBytes);
+                mbar_arrive_expect_tx(&full[i], kStageTx);
                 tma_load_2d_hint(sW + i * kWBytes, &tmW, &full[i], (kb0 + i) * BK, n0, stream_once);
             }
             const int warm = nkb < kL2Warm ? nkb : kL2Warm;
             for (int i = pre; i < warm; ++i) tma_prefetch_l2_2d(&tmW, (kb0 + i) * BK, n0);
             if (splits > 1) cluster_wait_acquire();
             grid_dep_wait();
-            if (FUSED) {
-                // The activation codes are written by the CTAs of this grid
-                // (generic stores) and read here by TMA: wait until every CTA
-                // has passed the grid barrier, then order the async-proxy
-                // reads after it. The loads are issued even if the wait gave
-                // up (the codes are then stale, and the error is recorded), so
-                // that every stage still completes and drains.
-                mbar_wait(qready, 0, abort_flag, err, kSiteQuantReady);
-                fence_proxy_async_global();
-            }
-            for (int i = 0; i < pre; ++i) tma_load_2d(sX + i * kXBytes, &tmX, &full[i], (kb0 + i) * BK, 0);
+            if (!FUSED)
+                for (int i = 0; i < pre; ++i) tma_load_2d(sX + i * kXBytes, &tmX, &full[i], (kb0 + i) * BK, 0);
             uint32_t stage = static_cast<uint32_t>(pre % kStages), phase = pre == kStages ? 1u : 0u;
             int issued = pre;
             for (int kb = kb0 + pre; kb < kb1; ++kb) {
                 if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err, kSiteProdEmpty)) break;
-                mbar_arrive_expect_tx(&full[stage], kWBytes + kXBytes);
+                mbar_arrive_expect_tx(&full[stage], kStageTx);
                 tma_load_2d_hint(sW + stage * kWBytes, &tmW, &full[stage], kb * BK, n0, stream_once);
-                tma_load_2d(sX + stage * kXBytes, &tmX, &full[stage], kb * BK, 0);
+                if (!FUSED) tma_load_2d(sX + stage * kXBytes, &tmX, &full[stage], kb * BK, 0);
                 ++issued;
                 if (++stage == kStages) { stage = 0; phase ^= 1u; }
             }
@@ -188,6 +200,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     tc_fence_after();
                 }
                 if (!mbar_wait<true>(&full[stage], phase, abort_flag, err, kSiteMmaFull)) break;
+                if (FUSED && !mbar_wait<true>(&xfull[stage], phase, abort_flag, err, kSiteMmaFull)) break;
                 tc_fence_after();
                 const uint32_t w0 = smem_u32(sW + stage * kWBytes);
                 const uint32_t x0 = smem_u32(sX + stage * kXBytes);
@@ -214,6 +227,74 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
             }
         }
+    } else if (FUSED && (warp == 2 || warp == 3)) {
+        // ------------------------------------------- activation quantizer --
+        // 64 threads per K block: thread t takes token row t/4 and the 16-code
+        // units 2(t%4), 2(t%4)+1 of the block's 8 (16 BF16 each); the row's
+        // amax is reduced over its four threads. The codes go to the stage's
+        // operand tile at the 128-byte-swizzled position the MMA descriptor
+        // reads (unit u of row r at unit u ^ (r % 8)), the scale to the ring.
+        const int t = threadIdx.x - 64;
+        const int row = t >> 2, u0 = (t & 3) * 2;
+        const bool has_row = row < M;
+        const bool writes_out = blockIdx.x < splits;  // the first row block's CTAs write qa and sa
+        grid_dep_wait();
+        uint32_t stage = 0, phase = 0;
+        bool go = true;
+        // X is read kQuantBatch K blocks at a time, all loads in flight
+        // together, so each batch costs one L2 round trip, not one per block.
+        for (int kbb = kb0; kbb < kb1 && go; kbb += kQuantBatch) {
+            uint4 v[kQuantBatch][4];
+#pragma unroll
+            for (int b = 0; b < kQuantBatch; ++b) {
+                const bool ld = has_row && kbb + b < kb1;
+                const uint16_t *src = fq.x + static_cast<int64_t>(row) * K + (kbb + b) * BK + u0 * 16;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) v[b][i] = ld ? ld_stream_v4(src + 8 * i) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int b = 0; b < kQuantBatch; ++b) {
+                const int kb = kbb + b;
+                if (kb >= kb1) break;
+                if (kb - kb0 >= kStages) {
+                    // Thread 0 waits for the stage to be free and decides for
+                    // all 64 (the decision is read after the barrier, and
+                    // rewritten only after the barrier that ends this block).
+                    if (t == 0)
+                        *quant_go = mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err, kSiteQuantEmpty) ? 1 : 0;
+                    named_bar_sync(3, 64);
+                    if (!*quant_go) {
+                        go = false;
+                        break;
+                    }
+                }
+                float a = fmaxf(fmaxf(amax8(v[b][0]), amax8(v[b][1])), fmaxf(amax8(v[b][2]), amax8(v[b][3])));
+                a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+                a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+                const float sc = block_scale(a);
+                const float rc = __frcp_rn(sc);
+                uint4 c[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint2 lo = quant8_recip(v[b][2 * h], sc, rc), hi = quant8_recip(v[b][2 * h + 1], sc, rc);
+                    c[h] = has_row ? make_uint4(lo.x, lo.y, hi.x, hi.y) : make_uint4(0u, 0u, 0u, 0u);
+                }
+                uint8_t *tile = sX + stage * kXBytes + row * BK;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) *reinterpret_cast<uint4 *>(tile + (((u0 + h) ^ (row & 7)) << 4)) = c[h];
+                if ((t & 3) == 0) xs_ring[(kb & (kXsRing - 1)) * kTok + row] = has_row ? sc : 0.0f;
+                if (writes_out && has_row) {
+                    uint8_t *dst = fq.qa_out + static_cast<int64_t>(row) * K + kb * BK + u0 * 16;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) *reinterpret_cast<uint4 *>(dst + 16 * h) = c[h];
+                    if ((t & 3) == 0) fq.sa_out[static_cast<int64_t>(kb) * M + row] = sc;
+                }
+                fence_proxy_async_smem();  // the MMA (async proxy) reads these shared-memory writes
+                named_bar_sync(3, 64);
+                if (t == 0) mbar_arrive(&xfull[stage]);
+                if (++stage == kStages) { stage = 0; phase ^= 1u; }
+            }
+        }
     } else if (warp >= 4) {
         // ---------------------------------------------------------- epilogue --
         const int ep = warp - 4;
@@ -221,29 +302,6 @@ __global__ void __launch_bounds__(kThreads, 2)
         const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(ep * 32) << 16);
         uint32_t buf = 0, bphase = 0;
         grid_dep_wait();
-        if (FUSED) {
-            // Fused activation quantization: the grid's CTAs take equal
-            // contiguous shares of the M x K/128 activation groups (in (row,
-            // group) order), a lane quad per group as in the stand-alone
-            // quantizer, and meet at a grid barrier before any CTA reads the
-            // codes. Every group is quantized exactly once.
-            const int64_t G = static_cast<int64_t>(M) * Kg;
-            const int64_t g0 = G * blockIdx.x / gridDim.x, g1 = G * (blockIdx.x + 1) / gridDim.x;
-            const int quad = (ep * 32 + lane) >> 2;
-            for (int64_t base = g0; base < g1; base += 32) {  // the same trip count in all four warps
-                const int64_t gi = base + quad;
-                const bool ok = gi < g1;
-                const int64_t m = ok ? gi / Kg : 0;
-                quant_group_by_quad(fq.x, fq.qa_out, const_cast<float *>(sa), M, K, m, ok ? gi - m * Kg : 0,
-                                    lane & 3, ok, [](const uint16_t *p) { return ld_stream_v4(p); });
-            }
-            named_bar_sync(2, 128);
-            if (ep == 0 && lane == 0) {
-                grid_barrier(fq.ws, gridDim.x, abort_flag, err, kSiteGridSync);
-                mbar_arrive(qready);
-            }
-            named_bar_sync(2, 128);
-        }
         if (!WHOLE_K) {
             // Scales of kScaleKb K blocks at a time go through this warp's own
             // shared-memory slice; the next chunk is loaded into registers while
@@ -257,10 +315,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                 for (int i = 0; i < kScaleKb * kTok / 32; ++i) {
                     const int idx = lane + 32 * i;
-                    const float *p = sa + static_cast<int64_t>(c0) * M + idx;
-                    // fused: sa is written by other CTAs of this grid, so not
-                    // through the read-only path
-                    r_sa[i] = idx < n * M ? (FUSED ? ld_cg_f32(p) : __ldg(p)) : 0.0f;
+                    // (fused: the activation scales come from the ring instead)
+                    r_sa[i] = (!FUSED && idx < n * M) ? __ldg(sa + static_cast<int64_t>(c0) * M + idx) : 0.0f;
                 }
                 r_sw = lane < n ? __ldg(swrow + c0 + lane) : 0.0f;
             };
@@ -276,12 +332,17 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const int c1 = min(kb1, c0 + kScaleKb);
                 for (int kb = c0; kb < c1; ++kb) {
                     const float wscale = w_sw[kb - c0];
-                    const float *srow = w_sa + (kb - c0) * M;
                     if (!__all_sync(0xffffffffu, mbar_wait(&tfull[buf], bphase, abort_flag, err, kSiteEpiFull))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
+                    // fused: the K block's MMA is complete, so its scales are in
+                    // the ring (written before the stage was marked full), and
+                    // the slot is not rewritten before this block's TMEM buffer
+                    // is released (the quantizer runs at most kStages + 1 K
+                    // blocks ahead of that).
+                    const float *srow = FUSED ? xs_ring + (kb & (kXsRing - 1)) * kTok : w_sa + (kb - c0) * M;
                     float p[kTok];
                     tmem_ld16(lane_addr + buf * kTok, p);
                     tc_fence_before();
@@ -467,30 +528,9 @@ cudaError_t launch_gemm_decode(const void *qa, const float *sa, const void *qw, 
     return launch_variant<kScaleBlock>(qa, sa, qw, sw, y, M, N, K, dev, stream);
 }
 
-bool decode_fused_fits(int64_t N, int64_t K, const DeviceInfo &dev) {
-    if (set_attributes<kScaleBlock, true>() != cudaSuccess) return false;
-    const int splits = pick_splits(N, K, dev);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(((N + kRows - 1) / kRows) * splits));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(splits);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, gemm_decode_kernel<kScaleBlock, true>, &cfg) != cudaSuccess)
-        return false;
-    return static_cast<int64_t>(clusters) >= (N + kRows - 1) / kRows;
-}
-
 cudaError_t launch_gemm_decode_fused(const void *x, void *qa, float *sa, const void *qw, const float *sw, void *y,
-                                     int64_t M, int64_t N, int64_t K, unsigned *ws, const DeviceInfo &dev,
-                                     cudaStream_t stream) {
-    const FusedQuant fq{static_cast<const uint16_t *>(x), static_cast<uint8_t *>(qa), ws};
+                                     int64_t M, int64_t N, int64_t K, const DeviceInfo &dev, cudaStream_t stream) {
+    const FusedQuant fq{static_cast<const uint16_t *>(x), static_cast<uint8_t *>(qa), sa};
     return launch_variant<kScaleBlock, true>(qa, sa, qw, sw, y, M, N, K, dev, stream, fq);
 }
 

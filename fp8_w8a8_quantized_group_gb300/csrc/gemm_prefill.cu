@@ -60,7 +60,7 @@ struct RegSplit {
 
 // Bounded-wait sites reported through the error word.
 enum : unsigned { kSiteProdEmpty = 101, kSiteMmaTmem = 102, kSiteMmaFull = 103, kSiteEpiFull = 104,
-                  kSiteDrain = 105, kSiteOffsets = 106, kSiteRowIndex = 107 };
+                  kSiteDrain = 105, kSiteOffsets = 106 };
 
 template <int BN>
 struct Cfg {
@@ -140,18 +140,12 @@ __device__ __forceinline__ uint4 pack8_scaled(const float *p, float s) {
     return v;
 }
 
-// GATHER (grouped block mode): row m of the problem reads activation row
-// row_index[m] of qa [M_src][K] (scales sa [K/128][M_src]); the A tile is
-// loaded by row-gather TMA, four rows per instruction, from all 32 lanes of
-// the producer warp.
-template <int BN, int MODE, bool GATHER = false>
+template <int BN, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const float *__restrict__ sa, const float *__restrict__ sw,
                         __nv_bfloat16 *__restrict__ y, int M, int N, int K, int groups,
-                        const int32_t *__restrict__ offsets, int raster, unsigned *err,
-                        const int32_t *__restrict__ row_index, int M_src) {
-    static_assert(!GATHER || MODE == kScaleBlock, "row gather is for the grouped block-scaled GEMM");
+                        const int32_t *__restrict__ offsets, int raster, unsigned *err) {
     using C = Cfg<BN>;
     constexpr bool WHOLE_K = MODE != kScaleBlock;  // all of K in one TMEM accumulator per tile
     constexpr uint32_t kIssuers = WHOLE_K ? 1u : 2u;  // MMA-issuing lanes
@@ -200,7 +194,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             t_start[groups] = acc;
             if (bad && blockIdx.x == 0) record_error(err, kErrArg, kSiteOffsets);
         }
-        if (GATHER) t_start[kMaxGroups + 1] = M_src;  // the activation-scale row stride of GATHER mode
     }
     if (warp == 0 && lane == 0) { tma_prefetch_desc(&tmA); tma_prefetch_desc(&tmB); }
     if (warp == 1) { tmem_alloc(tmem_slot, kTmemCols); tmem_relinquish(); }
@@ -217,59 +210,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp < 4) {
         regs_shrink<RegSplit<BN, WHOLE_K>::kLow>();
-        if (warp == 0 && (lane == 0 || GATHER)) {
+        if (warp == 0 && lane == 0) {
             // ------------------------------------------------ TMA producer --
             uint32_t stage = 0, phase = 0;
             int issued = 0;
-            if constexpr (!GATHER) {
-                for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
-                    const Tile tl = sched.get(t);
-                    for (int kb = 0; kb < Kg; ++kb) {
-                        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err, kSiteProdEmpty)) break;
-                        mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
-                        tma_load_2d(sA + stage * C::kABytes, &tmA, &full[stage], kb * BK, tl.m0);
-                        tma_load_2d(sB + stage * C::kBBytes, &tmB, &full[stage], kb * BK, tl.b_row);
-                        ++issued;
-                        if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
-                    }
-                }
-            } else {
-                // All 32 lanes: lane 0 waits and arms the stage, then every
-                // lane gathers four rows of the A tile.
-                bool live = true;  // lane 0's view, broadcast: warp-uniform
-                for (int t = blockIdx.x; t < total && live; t += gridDim.x) {
-                    const Tile tl = sched.get(t);
-                    for (int kb = 0; kb < Kg; ++kb) {
-                        if (lane == 0)
-                            live = !*abort_flag && mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err, kSiteProdEmpty);
-                        live = __shfl_sync(0xffffffffu, live, 0);
-                        if (!live) break;
-                        if (lane == 0) mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
-                        // This lane's four rows of the tile (re-read per K
-                        // block from L1 rather than held in registers); rows
-                        // past M read the map's fill value (row M_src lies
-                        // beyond its extent).
-                        int rows[4];
-                        bool bad = false;
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const int m = tl.m0 + 4 * lane + j;
-                            rows[j] = m < M ? __ldg(row_index + m) : M_src;
-                            bad |= m < M && (rows[j] < 0 || rows[j] >= M_src);
-                        }
-                        if (bad && kb == 0) record_error(err, kErrArg, kSiteRowIndex);
-                        __syncwarp();
-                        tma_gather4(sA + stage * C::kABytes + lane * 4 * BK, &tmA, &full[stage], kb * BK, rows[0],
-                                    rows[1], rows[2], rows[3]);
-                        if (lane == 0) tma_load_2d(sB + stage * C::kBBytes, &tmB, &full[stage], kb * BK, tl.b_row);
-                        ++issued;
-                        if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
-                    }
+            for (int t = blockIdx.x; t < total && !*abort_flag; t += gridDim.x) {
+                const Tile tl = sched.get(t);
+                for (int kb = 0; kb < Kg; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err, kSiteProdEmpty)) break;
+                    mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
+                    tma_load_2d(sA + stage * C::kABytes, &tmA, &full[stage], kb * BK, tl.m0);
+                    tma_load_2d(sB + stage * C::kBBytes, &tmB, &full[stage], kb * BK, tl.b_row);
+                    ++issued;
+                    if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
                 }
             }
             // Let the last fill of every stage land before the CTA can exit
             // (on the normal path these have all completed already).
-            for (int i = 0; i < C::kStages && i < issued && (!GATHER || lane == 0); ++i) {
+            for (int i = 0; i < C::kStages && i < issued; ++i) {
                 if (stage == 0) { stage = C::kStages; phase ^= 1u; }
                 --stage;
                 const uint64_t t0 = global_ns();
@@ -368,39 +326,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = 0; j < C::kCols; ++j) acc[j] = 0.0f;
                 const int nb = (tl.n0 + c0) / 128;  // this half lies in one 128-column weight block
                 const float *swp = sw + (static_cast<int64_t>(tl.group) * Nb + (nb < Nb ? nb : Nb - 1)) * Kg;
-                // Activation scales: row m's own, or (GATHER) those of its
-                // source row; in GATHER mode a row past M reads row 0's
-                // scales instead (it is not written).
-                // (GATHER reads the stride from shared memory at each use: one
-                // more live register here spills the 128-accumulator loop.)
-                const float *sap;
-                if constexpr (GATHER) {
-                    // A source row outside [0, M_src) (recorded by the producer)
-                    // reads zero codes and row 0's scales.
-                    const unsigned m_src = *reinterpret_cast<volatile unsigned *>(t_start + kMaxGroups + 1);
-                    const unsigned src = row_out ? static_cast<unsigned>(__ldg(row_index + m)) : 0u;
-                    sap = sa + min(src, m_src - 1u);
-                } else {
-                    sap = sa + m;
-                }
-                const bool sa_ok = GATHER || row_in;
+                const float *sap = sa + m;
                 // Scales of K blocks kb+1 and kb+2 are in flight while block kb is promoted.
-                float sa1 = sa_ok ? __ldg(sap) : 0.0f, sw1 = __ldg(swp);
-                float sa2, sw2 = Kg > 1 ? __ldg(swp + 1) : 0.0f;
-                if constexpr (GATHER)
-                    sa2 = Kg > 1 ? __ldg(sap + *reinterpret_cast<volatile int *>(t_start + kMaxGroups + 1)) : 0.0f;
-                else
-                    sa2 = (row_in && Kg > 1) ? __ldg(sap + M) : 0.0f;
+                float sa1 = row_in ? __ldg(sap) : 0.0f, sw1 = __ldg(swp);
+                float sa2 = (row_in && Kg > 1) ? __ldg(sap + M) : 0.0f, sw2 = Kg > 1 ? __ldg(swp + 1) : 0.0f;
                 for (int kb = 0; kb < Kg; ++kb) {
                     const float sc = sa1 * sw1;
                     sa1 = sa2;
                     sw1 = sw2;
                     if (kb + 2 < Kg) {
-                        if constexpr (GATHER)
-                            sa2 = __ldg(sap + static_cast<int64_t>(kb + 2) *
-                                                  *reinterpret_cast<volatile int *>(t_start + kMaxGroups + 1));
-                        else
-                            sa2 = row_in ? __ldg(sap + static_cast<int64_t>(kb + 2) * M) : 0.0f;
+                        sa2 = row_in ? __ldg(sap + static_cast<int64_t>(kb + 2) * M) : 0.0f;
                         sw2 = __ldg(swp + kb + 2);
                     }
                     ok = __all_sync(0xffffffffu, mbar_wait(&tfull[buf], bphase, abort_flag, err, kSiteEpiFull));
@@ -484,23 +419,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int BN, int MODE, bool GATHER = false>
+template <int BN, int MODE>
 cudaError_t launch_variant(const void *qa, const float *sa, const void *qw, const float *sw, void *y, int64_t M,
                            int64_t N, int64_t K, int num_groups, const int32_t *offsets, const DeviceInfo &dev,
-                           cudaStream_t stream, const int32_t *row_index = nullptr, int64_t M_src = 0) {
+                           cudaStream_t stream) {
     using C = Cfg<BN>;
     static std::once_flag attr_once[64];
     static cudaError_t attr_err[64];
     int device = 0;
     cudaGetDevice(&device);
     std::call_once(attr_once[device & 63], [&] {
-        cudaError_t e = cudaFuncSetAttribute(gemm_prefill_kernel<BN, MODE, GATHER>,
+        cudaError_t e = cudaFuncSetAttribute(gemm_prefill_kernel<BN, MODE>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
         // The register re-split inside the kernel needs the launch to hold at
         // least 128 * kLow + 256 * kHigh registers; refuse otherwise.
         using S = RegSplit<BN, MODE != kScaleBlock>;
         cudaFuncAttributes fa;
-        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, gemm_prefill_kernel<BN, MODE, GATHER>);
+        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, gemm_prefill_kernel<BN, MODE>);
         if (e == cudaSuccess && fa.numRegs * kThreads < 128 * S::kLow + 256 * S::kHigh)
             e = cudaErrorInvalidConfiguration;
         attr_err[device & 63] = e;
@@ -508,11 +443,7 @@ cudaError_t launch_variant(const void *qa, const float *sa, const void *qw, cons
     if (attr_err[device & 63] != cudaSuccess) return attr_err[device & 63];
 
     CUtensorMap tmA, tmB;
-    if (GATHER) {
-        if (encode_tma_2d_u8(&tmA, qa, K, M_src, K, BK, 1) != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    } else if (encode_tma_2d_u8(&tmA, qa, K, M, K, BK, BM) != CUDA_SUCCESS) {
-        return cudaErrorInvalidValue;
-    }
+    if (encode_tma_2d_u8(&tmA, qa, K, M, K, BK, BM) != CUDA_SUCCESS) return cudaErrorInvalidValue;
     const int64_t b_rows = N * (offsets != nullptr ? num_groups : 1);
     if (encode_tma_2d_u8(&tmB, qw, K, b_rows, K, BK, BN) != CUDA_SUCCESS) return cudaErrorInvalidValue;
 
@@ -525,9 +456,9 @@ cudaError_t launch_variant(const void *qa, const float *sa, const void *qw, cons
     // Tiles sharing a row panel run together when the weight operand is the
     // smaller one (it stays in L2 while activations stream), else the reverse.
     const int raster = (N <= M) ? 0 : 1;
-    gemm_prefill_kernel<BN, MODE, GATHER><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(
+    gemm_prefill_kernel<BN, MODE><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(
         tmA, tmB, sa, sw, static_cast<__nv_bfloat16 *>(y), static_cast<int>(M), static_cast<int>(N),
-        static_cast<int>(K), num_groups, offsets, raster, dev.err, row_index, static_cast<int>(M_src));
+        static_cast<int>(K), num_groups, offsets, raster, dev.err);
     return cudaGetLastError();
 }
 
@@ -547,17 +478,6 @@ cudaError_t launch_gemm_prefill(const void *qa, const float *sa, const void *qw,
     if (mode == kScaleRowCol) FP8_PREFILL_LAUNCH(kScaleRowCol);
     FP8_PREFILL_LAUNCH(kScaleBlock);
 #undef FP8_PREFILL_LAUNCH
-}
-
-cudaError_t launch_gemm_prefill_gather(const void *qa, const float *sa, const int32_t *row_index, int64_t M_src,
-                                       const void *qw, const float *sw, void *y, int64_t M, int64_t N, int64_t K,
-                                       int num_groups, const int32_t *offsets, const DeviceInfo &dev,
-                                       cudaStream_t stream) {
-    if (pick_bn(N) == 256)
-        return launch_variant<256, kScaleBlock, true>(qa, sa, qw, sw, y, M, N, K, num_groups, offsets, dev, stream,
-                                                      row_index, M_src);
-    return launch_variant<128, kScaleBlock, true>(qa, sa, qw, sw, y, M, N, K, num_groups, offsets, dev, stream,
-                                                  row_index, M_src);
 }
 
 }  // namespace fp8k

@@ -10,11 +10,11 @@
 // paged cache addresses slot = block * block_size + offset.
 //
 // Both kernels are HBM-bound (2 B read + 1 B written per element to store,
-// 1 B read + 2 B written to load): one CTA row per token, 16-byte BF16 loads
-// and 8-byte code stores (store), 8-byte code loads and 16-byte BF16 stores
-// (load). Codes are e4m3(fl32(x / scale)) through one reciprocal per tensor
-// with the exact fallback of quant8_recip; dequantized values are
-// bf16(fl32(dec(q) * scale)).
+// 1 B read + 2 B written to load): a grid-stride loop of CTAs over token rows,
+// 16-byte BF16 loads and 8-byte code stores (store), 8-byte code loads and
+// 16-byte BF16 stores (load). Codes are e4m3(fl32(x / scale)) through one
+// reciprocal per tensor with the exact fallback of quant8_recip; dequantized
+// values are bf16(fl32(dec(q) * scale)).
 #include "common.cuh"
 #include "launch.h"
 

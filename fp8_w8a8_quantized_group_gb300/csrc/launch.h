@@ -20,8 +20,11 @@ struct DeviceInfo {
 CUresult encode_tma_2d_u8(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
                           uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows);
 
+// 1x128 activation groups. row_index (device int32 [M], or nullptr): row m of
+// q / s is quantized from row row_index[m] of x [M_src][K] (M_src = M without).
 cudaError_t launch_quant_act_group(const void *x, void *q, float *s, int64_t M, int64_t K,
-                                   const DeviceInfo &dev, cudaStream_t stream);
+                                   const DeviceInfo &dev, cudaStream_t stream,
+                                   const int32_t *row_index = nullptr, int64_t M_src = 0);
 cudaError_t launch_quant_weight_block(const void *w, void *q, float *s, int64_t N, int64_t K,
                                       const DeviceInfo &dev, cudaStream_t stream);
 // One scale per row of x [rows][cols] (per-token activations, per-channel weights).
@@ -51,26 +54,16 @@ cudaError_t launch_gemm_prefill(const void *qa, const float *sa, const void *qw,
                                 int64_t M, int64_t N, int64_t K, int num_groups, const int32_t *offsets,
                                 ScaleMode mode, const DeviceInfo &dev, cudaStream_t stream);
 
-// The grouped block-scaled prefill GEMM with a row gather: row m of the
-// problem is row row_index[m] of qa [M_src][K] (scales sa [K/128][M_src]).
-cudaError_t launch_gemm_prefill_gather(const void *qa, const float *sa, const int32_t *row_index, int64_t M_src,
-                                       const void *qw, const float *sw, void *y, int64_t M, int64_t N, int64_t K,
-                                       int num_groups, const int32_t *offsets, const DeviceInfo &dev,
-                                       cudaStream_t stream);
-
 // Weight-streaming tcgen05 GEMM for M <= 16 (weights as the MMA's M side).
 cudaError_t launch_gemm_decode(const void *qa, const float *sa, const void *qw, const float *sw, void *y,
                                int64_t M, int64_t N, int64_t K, ScaleMode mode, const DeviceInfo &dev,
                                cudaStream_t stream);
 
 // The decode GEMM with the 1x128 activation quantization fused in (M <= 16,
-// block mode): every CTA quantizes a share of x into qa / sa, the grid meets
-// at a barrier kept in ws (two zeroed words), then the GEMM reads the codes.
-// Only valid when decode_fused_fits(): every CTA of the grid resident at once.
-bool decode_fused_fits(int64_t N, int64_t K, const DeviceInfo &dev);
+// block mode): two warps of every CTA quantize each K block of x into the
+// shared-memory operand stage; the first row block's CTAs also write qa / sa.
 cudaError_t launch_gemm_decode_fused(const void *x, void *qa, float *sa, const void *qw, const float *sw, void *y,
-                                     int64_t M, int64_t N, int64_t K, unsigned *ws, const DeviceInfo &dev,
-                                     cudaStream_t stream);
+                                     int64_t M, int64_t N, int64_t K, const DeviceInfo &dev, cudaStream_t stream);
 
 // One CTA whose waits never complete: the first gives up after the wait limit
 // and records FP8_ERR_TIMEOUT (site 901); the second returns at the abort flag.

@@ -30,7 +30,7 @@ namespace fp8k {
 namespace {
 
 // Error-word sites of the device-side argument checks.
-enum : unsigned { kSiteStaticScale = 301, kSiteStaticScaleSmall = 302 };
+enum : unsigned { kSiteStaticScale = 301, kSiteStaticScaleSmall = 302, kSiteRowIndex = 303 };
 
 // ------------------------------------------------ 1 x 128 activation groups --
 
@@ -47,10 +47,13 @@ constexpr int kActGroups = 8;               // groups per CTA: one lane quad eac
 // group 8*blockIdx.y + j). Lane c of a quad holds the 16-byte chunks
 // c, c+4, c+8, c+12 of the group's 256 bytes, so each warp-wide load covers
 // 64 contiguous bytes of every group and each store 32.
+template <bool GATHER>
 __global__ void __launch_bounds__(kActThreads, 6) quant_act_group_kernel(const uint16_t *__restrict__ x,
                                                                       uint8_t *__restrict__ q,
                                                                       float *__restrict__ s, int64_t M,
-                                                                      int64_t K) {
+                                                                      int64_t K,
+                                                                      const int32_t *__restrict__ row_index,
+                                                                      int64_t M_src, unsigned *err) {
     const int64_t Kg = K / 128;
     const int lane = threadIdx.x & 31;
     const int c = lane & 3;
@@ -63,7 +66,17 @@ __global__ void __launch_bounds__(kActThreads, 6) quant_act_group_kernel(const u
     grid_dep_wait();
 
     const int64_t g = static_cast<int64_t>(blockIdx.y) * kActGroups + (lane >> 2);
-    quant_group_by_quad(x, q, s, M, K, m, g, c, m < M && g < Kg, [](const uint16_t *p) { return ld_stream_v4(p); });
+    int64_t src = m;
+    if (GATHER && m < M) {
+        // Routed row m reads source row row_index[m]; one outside [0, M_src)
+        // is recorded and reads row 0 instead.
+        const int r = __ldg(row_index + m);
+        const bool bad = r < 0 || static_cast<int64_t>(r) >= M_src;
+        if (bad && lane == 0 && blockIdx.y == 0) record_error(err, kErrArg, kSiteRowIndex);
+        src = bad ? 0 : r;
+    }
+    quant_group_by_quad(x, q, s, M, K, m, src, g, c, m < M && g < Kg,
+                        [](const uint16_t *p) { return ld_stream_v4(p); });
 }
 
 // --------------------------------------------------- 128 x 128 weight blocks --
@@ -311,8 +324,8 @@ cudaError_t launch_quant_rows(const void *x, void *q, float *s, int64_t rows, in
 }
 
 cudaError_t launch_quant_act_group(const void *x, void *q, float *s, int64_t M, int64_t K,
-                                   const DeviceInfo &dev, cudaStream_t stream) {
-    (void)dev;
+                                   const DeviceInfo &dev, cudaStream_t stream, const int32_t *row_index,
+                                   int64_t M_src) {
     const int64_t rows = (M + kActRows - 1) / kActRows;
     const int64_t cols = (K / 128 + kActGroups - 1) / kActGroups;
     if (rows == 0 || cols == 0) return cudaSuccess;
@@ -326,8 +339,11 @@ cudaError_t launch_quant_act_group(const void *x, void *q, float *s, int64_t M, 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, quant_act_group_kernel, static_cast<const uint16_t *>(x),
-                              static_cast<uint8_t *>(q), s, M, K);
+    if (row_index != nullptr)
+        return cudaLaunchKernelEx(&cfg, quant_act_group_kernel<true>, static_cast<const uint16_t *>(x),
+                                  static_cast<uint8_t *>(q), s, M, K, row_index, M_src, dev.err);
+    return cudaLaunchKernelEx(&cfg, quant_act_group_kernel<false>, static_cast<const uint16_t *>(x),
+                              static_cast<uint8_t *>(q), s, M, K, row_index, M, dev.err);
 }
 
 cudaError_t launch_quant_weight_block(const void *w, void *q, float *s, int64_t N, int64_t K,

@@ -98,6 +98,18 @@ def fp8_quant_act_group(x, q, scales, group_k: int = GROUP, stream=None) -> None
     _check(_lib.load().fp8_quant_act_group(*args, M, K, group_k, _stream(stream)), "fp8_quant_act_group")
 
 
+def fp8_quant_act_group_gather(x, row_index, q, scales, group_k: int = GROUP, stream=None) -> None:
+    """Routed rows: q[m] (and its scales) = the quantization of x[row_index[m]]."""
+    M_src, K = x.shape
+    M = row_index.shape[0]
+    _need(q, M * K, "q")
+    _need(scales, (K // group_k if group_k > 0 else 0) * M, "scales")
+    xp, ri, qp, sp = _ptrs((x, torch.bfloat16, "x"), (row_index, torch.int32, "row_index"), (q, CODES, "q"),
+                           (scales, torch.float32, "scales"))
+    _check(_lib.load().fp8_quant_act_group_gather(xp, ri, qp, sp, M, M_src, K, group_k, _stream(stream)),
+           "fp8_quant_act_group_gather")
+
+
 def fp8_quant_weight_block(w, q, scales, block_n: int = GROUP, block_k: int = GROUP, stream=None) -> None:
     N, K = w.shape
     _need(q, N * K, "q")
@@ -133,24 +145,6 @@ def fp8_block_gemm(qa, sa, qw, sw, y, block_n: int = GROUP, block_k: int = GROUP
                                       _stream(stream)), "fp8_block_gemm")
 
 
-def fp8_block_gemm_gather(qa, sa, row_index, qw, sw, y, group_offsets, stream=None) -> None:
-    """Grouped GEMM over routed rows: row m reads row row_index[m] of qa [M_src, K]."""
-    M_src, K = qa.shape
-    M = row_index.shape[0]
-    N = y.shape[1]
-    G = qw.shape[0] if qw.dim() == 3 else 1
-    _need(sa, _cdiv(K, GROUP) * M_src, "sa")
-    _need(qw, G * N * K, "qw")
-    _need(sw, G * _cdiv(N, GROUP) * _cdiv(K, GROUP), "sw")
-    _need(y, M * N, "y")
-    _need(group_offsets, G + 1, "group_offsets")
-    args = _ptrs((qa, CODES, "qa"), (sa, torch.float32, "sa"), (row_index, torch.int32, "row_index"),
-                 (qw, CODES, "qw"), (sw, torch.float32, "sw"), (y, torch.bfloat16, "y"),
-                 (group_offsets, torch.int32, "group_offsets"))
-    _check(_lib.load().fp8_block_gemm_gather(args[0], args[1], args[2], M_src, args[3], args[4], args[5], M, N, K,
-                                             G, args[6], _stream(stream)), "fp8_block_gemm_gather")
-
-
 def fp8_tensor_gemm(qa, sa, qw, sw, y, stream=None) -> None:
     M, K = qa.shape
     N = y.shape[1]
@@ -174,29 +168,6 @@ def fp8_block_linear(x, qa, sa, qw, sw, y, stream=None) -> None:
     args = _ptrs((x, torch.bfloat16, "x"), (qa, CODES, "qa"), (sa, torch.float32, "sa"), (qw, CODES, "qw"),
                  (sw, torch.float32, "sw"), (y, torch.bfloat16, "y"))
     _check(_lib.load().fp8_block_linear(*args, M, N, K, _stream(stream)), "fp8_block_linear")
-
-
-FUSED_WORKSPACE_BYTES = 8
-
-
-def fused_workspace(device=None) -> torch.Tensor:
-    """A zeroed workspace for fp8_block_linear_fused (one per stream)."""
-    return torch.zeros(FUSED_WORKSPACE_BYTES // 4, dtype=torch.int32, device=device or "cuda")
-
-
-def fp8_block_linear_fused(x, qa, sa, qw, sw, y, workspace, stream=None) -> None:
-    M, K = x.shape
-    N = y.shape[1]
-    _need(qa, M * K, "qa")
-    _need(sa, _cdiv(K, GROUP) * M, "sa")
-    _need(qw, N * K, "qw")
-    _need(sw, _cdiv(N, GROUP) * _cdiv(K, GROUP), "sw")
-    _need(y, M * N, "y")
-    args = _ptrs((x, torch.bfloat16, "x"), (qa, CODES, "qa"), (sa, torch.float32, "sa"), (qw, CODES, "qw"),
-                 (sw, torch.float32, "sw"), (y, torch.bfloat16, "y"), (workspace, torch.int32, "workspace"))
-    ws_bytes = workspace.numel() * 4
-    _check(_lib.load().fp8_block_linear_fused(*args[:6], M, N, K, args[6], ws_bytes, _stream(stream)),
-           "fp8_block_linear_fused")
 
 
 def fp8_quant_rowwise(x, q, scales, stream=None) -> None:
@@ -337,17 +308,6 @@ def rowwise_gemm(qa, sa, qw, sw, stream=None) -> torch.Tensor:
     y = torch.empty((qa.shape[0], qw.shape[0]), dtype=torch.bfloat16, device=qa.device)
     fp8_rowwise_gemm(qa, sa, qw, sw, y, stream=stream)
     return y
-
-
-def block_linear_fused(x, qw, sw, workspace, stream=None):
-    """As block_linear, through fp8_block_linear_fused with the given workspace."""
-    M, K = x.shape
-    N = qw.shape[0]
-    qa = torch.empty((M, K), dtype=torch.uint8, device=x.device)
-    sa = torch.empty((K // GROUP, M), dtype=torch.float32, device=x.device)
-    y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
-    fp8_block_linear_fused(x, qa, sa, qw, sw, y, workspace, stream=stream)
-    return y, qa, sa
 
 
 def tensor_gemm(qa, sa, qw, sw, stream=None) -> torch.Tensor:

@@ -52,13 +52,12 @@
  * let the next kernel launch before they complete (griddepcontrol.
  * launch_dependents). A dependent always waits for its predecessor to
  * complete before it reads that predecessor's outputs - with one exception:
- * the decode GEMM (fp8_block_gemm dense, fp8_tensor_gemm, fp8_rowwise_gemm,
- * fp8_block_linear and fp8_block_linear_fused, each with M <= 16) starts
- * loading qw before that wait.
+ * the decode GEMM (fp8_block_gemm dense, fp8_tensor_gemm, fp8_rowwise_gemm
+ * and fp8_block_linear, each with M <= 16) starts loading qw before that wait.
  * So qw must not be written by a kernel that lets its dependents launch
  * early. Per entry point:
  *    fp8_quant_act_group     lets its dependent launch early (its q and s are
- *                            written after that): never use its codes as the
+ *    (and _gather)           written after that): never use its codes as the
  *                            qw of a decode GEMM enqueued directly after it;
  *    fp8_quant_weight_block  does not (qw from it is safe);
  *    fp8_quant_per_tensor    does not, static or dynamic: its last kernel
@@ -67,11 +66,9 @@
  *    decode GEMM             lets its dependent launch early; it writes y
  *                            after its own wait, and reads only qw early;
  *    prefill GEMM            does not;
- *    fp8_block_linear        its quantizer lets its own GEMM launch early (the
- *                            GEMM reads qa and sa after its wait); its GEMM is
- *                            the decode or prefill GEMM above;
- *    fp8_block_linear_fused  as the decode GEMM (one kernel), or as
- *                            fp8_block_linear where it falls back to it.
+ *    fp8_block_linear        M <= 16: one kernel, as the decode GEMM; M > 16:
+ *                            its quantizer lets the prefill GEMM launch early
+ *                            (that GEMM does not read before its wait).
  * Work that is not this library's (torch kernels, copies) never triggers
  * early, so a plain stream order with it is always safe.
  */
@@ -119,6 +116,28 @@ enum fp8_status {
  */
 int fp8_quant_act_group(const void *x_bf16, void *q_e4m3, float *scales,
                         int64_t M, int64_t K, int group_k, void *stream);
+
+/*
+ * Activation quantization of routed rows (mixture of experts): row m of the
+ * output is row row_index[m] of x quantized as fp8_quant_act_group does, so the
+ * expert-sorted codes that the grouped fp8_block_gemm reads are written
+ * straight from the token-order activations, with no permuted copy of x
+ * (Fp8MoEMethod of "[vLLM] FP8", section "Fp8Config: 온라인 vs 오프라인"; the
+ * routing itself is the caller's). Quantization is per row, so the codes and
+ * scales equal fp8_quant_act_group's on the permuted rows, bit for bit.
+ *
+ *   x_bf16     [M_src][K] BF16, input, token order.
+ *   row_index  DEVICE int32 [M]: the source row of each routed row. A value
+ *              outside [0, M_src) is recorded as FP8_ERR_ARG (site 303) in
+ *              the device error word and reads row 0.
+ *   q_e4m3     [M][K] E4M3, scales [K/128][M] FP32: outputs, routed order.
+ *   group_k must be 128; K a positive multiple of 128 up to
+ *   FP8_ACT_GROUP_MAX_K; M >= 0; M_src >= 1 when M > 0.
+ * PDL: as fp8_quant_act_group.
+ * Errors: NULL, SHAPE, ALIGN, UNSUPPORTED, DEVICE, CUDA.
+ */
+int fp8_quant_act_group_gather(const void *x_bf16, const int32_t *row_index, void *q_e4m3, float *scales,
+                               int64_t M, int64_t M_src, int64_t K, int group_k, void *stream);
 
 /*
  * Weight block quantization (offline, at load time), one scale per 128 x 128
@@ -194,34 +213,6 @@ int fp8_block_gemm(const void *qa, const float *sa, const void *qw, const float 
                    void *y_bf16, int64_t M, int64_t N, int64_t K,
                    int block_n, int block_k, int group_k,
                    int num_groups, const int32_t *group_offsets, void *stream);
-
-/*
- * Grouped (mixture-of-experts) block-scaled GEMM that gathers its activation
- * rows: row m of the problem is row row_index[m] of the token-order codes, so
- * the routed (expert-sorted) activations are never materialised
- * (Fp8MoEMethod of "[vLLM] FP8", section "Fp8Config: 온라인 vs 오프라인"; the
- * routing itself is the caller's). Same formula as fp8_block_gemm, grouped:
- *   Y[m,n] = bf16( sum_g Sa[g][r] Sw_e[n/128][g] sum_{k in g} dec(Qa[r,k]) dec(Qw_e[n,k]) ),
- *   r = row_index[m], e the expert whose range holds m.
- *
- *   qa         [M_src][K] E4M3 and sa [K/128][M_src] FP32: the tokens'
- *              codes and scales in token order (fp8_quant_act_group on X).
- *   row_index  DEVICE int32 [M], 16-byte aligned: the source row of each
- *              routed row. Values outside [0, M_src) read zero codes and are
- *              recorded as FP8_ERR_ARG (site 107) in the device error word.
- *   qw, sw     [num_groups][N][K] and [num_groups][ceil(N/128)][K/128].
- *   y          [M][N] BF16, output, routed order.
- *   group_offsets  DEVICE int32 [num_groups+1] over the M routed rows, as in
- *              fp8_block_gemm (required here); rows outside all experts are
- *              not written.
- *   K a positive multiple of 128, N a positive multiple of 16, M >= 0,
- *   M_src >= 1, num_groups in [1, FP8_MAX_GROUPS].
- * The A tiles are loaded by row-gather TMA (four rows per instruction).
- * Errors: NULL, SHAPE, ALIGN, UNSUPPORTED, ARG, DEVICE, CUDA.
- */
-int fp8_block_gemm_gather(const void *qa, const float *sa, const int32_t *row_index, int64_t M_src,
-                          const void *qw, const float *sw, void *y_bf16, int64_t M, int64_t N, int64_t K,
-                          int num_groups, const int32_t *group_offsets, void *stream);
 
 /*
  * Per-tensor FP8 GEMM: Y[m,n] = bf16( sa * sw * sum_k dec(Qa[m,k]) dec(Qw[n,k]) ),
@@ -323,48 +314,22 @@ int fp8_kv_cache_load(const void *key_cache, const void *value_cache, void *key_
  *           and scales (caller-owned; bit-identical to fp8_quant_act_group).
  *   qw, sw  as fp8_block_gemm (block_n = block_k = group_k = 128).
  *   y       [M][N] BF16, output.
- *   K a positive multiple of 128, N a positive multiple of 16, M >= 0.
- * Two launches on `stream`: the quantization kernel, then the decode
- * (M <= 16) or prefill GEMM. The quantization kernel is a programmatic
- * dependent of the work before it, and the GEMM of the quantization kernel:
- * each starts its prologue (and the decode GEMM loads its first weights)
- * while its predecessor finishes, and waits for it before reading its output.
+ *   K a positive multiple of 128 up to FP8_ACT_GROUP_MAX_K, N a positive
+ *   multiple of 16, M >= 0.
+ * M <= 16 (decode): ONE launch. The activation quantization runs inside the
+ * decode GEMM kernel: two warps of every CTA quantize each K block of X into
+ * the shared-memory operand stage the MMA reads (the quantize/dequantize
+ * overhead of "FP8 Quantization", section E, item 4, kept off the critical
+ * path: no separate kernel, no round trip of the codes through memory, no
+ * grid-wide wait). The CTAs of the first 128-row weight block also write qa
+ * and sa, each group exactly once.
+ * M > 16 (prefill): two launches, the quantization kernel then the prefill
+ * GEMM; the quantization kernel is a programmatic dependent of the work
+ * before it.
  * Errors: NULL, SHAPE, ALIGN, DEVICE, CUDA.
  */
 int fp8_block_linear(const void *x_bf16, void *qa, float *sa, const void *qw, const float *sw,
                      void *y_bf16, int64_t M, int64_t N, int64_t K, void *stream);
-
-/* Bytes of caller workspace fp8_block_linear_fused needs. */
-#define FP8_FUSED_WORKSPACE_BYTES 8
-
-/*
- * W8A8 linear layer with the activation quantization inside the GEMM kernel,
- * for decode (M <= 16). fp8_block_linear runs the quantizer as a kernel of its
- * own, and at decode sizes that kernel is a latency step in every layer's
- * dependency chain - the quantize/dequantize overhead that "FP8 Quantization"
- * (section E, item 4) names as what can eat FP8's gain. Here every CTA of the
- * decode GEMM quantizes an equal share of X's 1x128 groups (each group
- * exactly once), the CTAs meet at a bounded grid-wide barrier, and then the
- * GEMM reads the codes. qa, sa and y are bit-identical to fp8_block_linear's.
- *
- *   x_bf16, qa, sa, qw, sw, y, M, N, K  as fp8_block_linear.
- *   workspace        DEVICE memory, at least FP8_FUSED_WORKSPACE_BYTES bytes,
- *                    4-byte aligned, caller-owned: the barrier's counters. It
- *                    must be zeroed once before first use; each call leaves it
- *                    ready for the next. Calls that may run at the same time
- *                    (on different streams) need different workspaces. After a
- *                    call that reports FP8_ERR_TIMEOUT it must be zeroed again.
- *   workspace_bytes  its size in bytes.
- * The barrier needs every CTA of the GEMM resident at once. When the shape
- * does not allow that, or M > 16, the call runs fp8_block_linear's two
- * kernels instead (same results; the workspace is not touched). A barrier
- * wait longer than about one second gives up and records FP8_ERR_TIMEOUT
- * (site 207) in the device error word.
- * Errors: NULL, SHAPE, ALIGN, ARG (workspace too small), DEVICE, CUDA.
- */
-int fp8_block_linear_fused(const void *x_bf16, void *qa, float *sa, const void *qw, const float *sw,
-                           void *y_bf16, int64_t M, int64_t N, int64_t K, void *workspace,
-                           int64_t workspace_bytes, void *stream);
 
 /* Static, NUL-terminated description of a status code. Never NULL. */
 const char *fp8_status_string(int status);

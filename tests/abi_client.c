@@ -116,19 +116,6 @@ int main(void)
            FP8_ERR_ALIGN);
     EXPECT(fp8_kv_cache_load(NULL, NULL, NULL, NULL, NULL, NULL, NULL, 0, 128, 8, NULL), FP8_OK);
 
-    /* the fused linear layer: its workspace is required and sized */
-    EXPECT(fp8_block_linear_fused(FAKE, FAKE, FAKE_F, FAKE, FAKE_F, FAKE, 4, 256, 256, NULL, 64, NULL),
-           FP8_ERR_NULL);
-    EXPECT(fp8_block_linear_fused(FAKE, FAKE, FAKE_F, FAKE, FAKE_F, FAKE, 4, 256, 256, FAKE,
-                                  FP8_FUSED_WORKSPACE_BYTES - 4, NULL),
-           FP8_ERR_ARG);
-    EXPECT(fp8_block_linear_fused(FAKE, FAKE, FAKE_F, FAKE, FAKE_F, FAKE, 4, 256, 256, ODD2_F,
-                                  FP8_FUSED_WORKSPACE_BYTES, NULL),
-           FP8_ERR_ALIGN);
-    EXPECT(fp8_block_linear_fused(FAKE, FAKE, FAKE_F, FAKE, FAKE_F, FAKE, 4, 256, 200, FAKE,
-                                  FP8_FUSED_WORKSPACE_BYTES, NULL),
-           FP8_ERR_SHAPE);
-
     /* the conversion self-test: n a multiple of 8, no pattern past 0xFFFFFFFF */
     EXPECT(fp8_selftest_encode_f32(0, 12, FAKE, NULL), FP8_ERR_SHAPE);
     EXPECT(fp8_selftest_encode_f32(0, -8, FAKE, NULL), FP8_ERR_SHAPE);

@@ -347,27 +347,25 @@ def test_rowwise_gemm_full_size(M, N, K):
     assert_within_tolerance(yg[ms, ns], yo, ab, f"rowwise {M}x{N}x{K} sampled")
 
 
-# ---------------------------------------- fused activation quantization --
+# ---------------------------------- activation quantization in the GEMM --
 
-@pytest.mark.parametrize("M,N,K", [(1, 256, 256), (3, 384, 1024), (16, 4096, 4096), (7, 272, 14336),
-                                   (1, 28672, 4096), (16, 6144, 4096), (5, 19584, 8320), (16, 4096, 14336),
-                                   (40, 512, 512)])
-def test_block_linear_fused_matches_separate_calls(M, N, K):
-    """fp8_block_linear_fused (one kernel: quantization inside the decode GEMM,
-    a grid barrier between) writes the same codes, scales and Y, bit for bit,
-    as fp8_quant_act_group followed by fp8_block_gemm; M > 16 takes the
-    two-kernel path. Y is within tolerance of the oracle on sampled points."""
+@pytest.mark.parametrize("M,N,K", [(16, 4096, 4096), (16, 6144, 4096), (16, 4096, 14336), (9, 1024, 1280),
+                                   (2, 19584, 8320), (16, 256, 128)])
+def test_block_linear_decode_is_one_kernel_matching_separate_calls(M, N, K):
+    """At M <= 16 fp8_block_linear quantizes inside the decode GEMM (two warps
+    fill each stage's operand tile; the first row block's CTAs write qa and
+    sa). Codes, scales and Y are bit-identical to fp8_quant_act_group followed
+    by fp8_block_gemm, here for K ranges of one to 65 blocks per CTA, split
+    and unsplit, and M not a multiple of four."""
     xd = synth.device_normal_bf16(M, K, 21, f"fused/X/{M}x{K}", outlier_cols=[3, K // 2], outlier_scale=50.0)
     wd = synth.device_normal_bf16(N, K, 21, f"fused/W/{N}x{K}", sigma=0.02)
     qw, sw = ops.quant_weight_block(wd)
-    ws = ops.fused_workspace()
-    y, qa, sa = ops.block_linear_fused(xd, qw, sw, ws)
+    y, qa, sa = ops.block_linear(xd, qw, sw)
     qa2, sa2 = ops.quant_act_group(xd)
     y2 = ops.block_gemm(qa2, sa2, qw, sw)
     assert ops.fp8_device_error() == (0, 0)
     assert torch.equal(qa, qa2) and torch.equal(sa.view(torch.int32), sa2.view(torch.int32))
     assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
-    assert int(ws[0].item()) == 0  # the barrier's arrival count is back at zero
     x = xd.view(torch.int16).cpu().numpy().view(np.uint16)
     qao, sao = oracle.quant_act_group(x)
     assert np.array_equal(qa.cpu().numpy(), qao) and np.array_equal(f32_bits(sa.cpu().numpy()), f32_bits(sao))
@@ -378,120 +376,88 @@ def test_block_linear_fused_matches_separate_calls(M, N, K):
         w_blk = wd[n0:n1].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
         qwo, swo = oracle.quant_weight_block(w_blk)
         yo, ab = oracle.gemm_block(qao, sao, qwo, swo)
-        assert_within_tolerance(bf16_to_f64(y)[:, n0:n1], yo, ab, f"fused {M}x{N}x{K} columns {n0}..{n1}")
+        assert_within_tolerance(bf16_to_f64(y)[:, n0:n1], yo, ab, f"linear {M}x{N}x{K} columns {n0}..{n1}")
 
 
-def test_block_linear_fused_back_to_back_one_workspace():
-    """Twenty fused calls on one stream with one workspace and fresh inputs,
-    no host sync: each matches the two-kernel path bit for bit."""
+def test_block_linear_back_to_back_no_sync():
+    """Twenty one-kernel linear calls on one stream, fresh activations, one
+    shared qa / sa pair (as a layer loop reuses them), no host sync: each Y
+    matches the two-kernel path bit for bit."""
     M, N, K = 16, 4096, 4096
     wd = synth.device_normal_bf16(N, K, 22, "fused/seq/W", sigma=0.02)
     qw, sw = ops.quant_weight_block(wd)
-    ws = ops.fused_workspace()
     xs = [synth.device_normal_bf16(M, K, i, f"fused/seq/X/{i}") for i in range(20)]
-    qa = torch.empty((M, K), dtype=torch.uint8, device="cuda")   # shared, as a layer loop reuses them
+    qa = torch.empty((M, K), dtype=torch.uint8, device="cuda")
     sa = torch.empty((K // 128, M), dtype=torch.float32, device="cuda")
     ys = [torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for _ in xs]
     torch.cuda.synchronize()
     for x, y in zip(xs, ys):
-        ops.fp8_block_linear_fused(x, qa, sa, qw, sw, y, ws)
+        ops.fp8_block_linear(x, qa, sa, qw, sw, y)
     assert ops.fp8_device_error() == (0, 0)
     for x, y in zip(xs, ys):
         qa2, sa2 = ops.quant_act_group(x)
         assert torch.equal(y.view(torch.int16), ops.block_gemm(qa2, sa2, qw, sw).view(torch.int16))
-    assert int(ws[0].item()) == 0
 
 
 # ------------------------------------------------------- gathered rows --
 
-def _gather_case(tokens, counts, N, K, seed):
-    """Token-order activations, a routing (row_index, offsets) with the given
-    per-expert counts, expert weights."""
-    rng = np.random.default_rng(seed)
-    counts = np.asarray(counts)
-    offsets = np.zeros(len(counts) + 1, dtype=np.int32)
-    offsets[1:] = np.cumsum(counts)
-    M = int(offsets[-1])
+def test_quant_gather_equals_quant_of_permuted_rows():
+    """Routed-row quantization reads each row through the index: codes and
+    scales equal fp8_quant_act_group on the permuted copy, and the oracle."""
+    rng = np.random.default_rng(3)
+    tokens, K = 700, 1152
+    M = 1301
     row_index = rng.integers(0, tokens, size=M).astype(np.int32)
-    x = synth.activations(tokens, K, seed, f"gather/{tokens}")
-    w = np.stack([synth.weights(N, K, seed, f"gather/W{e}") for e in range(len(counts))])
-    return x, w, row_index, offsets
-
-
-def test_gather_gemm_equals_grouped_gemm_on_permuted_rows():
-    """Row-gather TMA reads the same codes a pre-permuted copy holds: the
-    output equals fp8_block_gemm on qa[row_index], bit for bit, and the oracle
-    within tolerance."""
-    x, w, row_index, offsets = _gather_case(700, [5, 0, 300, 129, 1, 128, 263], N=256, K=512, seed=3)
-    E, N, K = w.shape
-    M = int(offsets[-1])
-    qa, sa = ops.quant_act_group(to_dev_bf16(x))
-    qw = torch.empty((E, N, K), dtype=torch.uint8, device="cuda")
-    sw = torch.empty((E, N // 128, K // 128), dtype=torch.float32, device="cuda")
-    for e in range(E):
-        ops.fp8_quant_weight_block(to_dev_bf16(w[e]), qw[e], sw[e])
+    x = synth.activations(tokens, K, 3, "gather/X", outlier_channels=2, outlier_scale=50.0)
+    xd = to_dev_bf16(x)
     ri = torch.from_numpy(row_index).cuda()
-    off = torch.from_numpy(offsets).cuda()
-    y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
-    ops.fp8_block_gemm_gather(qa, sa, ri, qw, sw, y, off)
-    qa_p = qa.index_select(0, ri.long()).contiguous()
-    sa_p = sa.index_select(1, ri.long()).contiguous()
-    y2 = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
-    ops.fp8_block_gemm(qa_p, sa_p, qw, sw, y2, num_groups=E, group_offsets=off)
+    q = torch.empty((M, K), dtype=torch.uint8, device="cuda")
+    s = torch.empty((K // 128, M), dtype=torch.float32, device="cuda")
+    ops.fp8_quant_act_group_gather(xd, ri, q, s)
+    q2, s2 = ops.quant_act_group(xd.index_select(0, ri.long()).contiguous())
     assert ops.fp8_device_error() == (0, 0)
-    assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
-    qao, sao = oracle.quant_act_group(x)
-    qwo = np.stack([oracle.quant_weight_block(w[e])[0] for e in range(E)])
-    swo = np.stack([oracle.quant_weight_block(w[e])[1] for e in range(E)])
-    ms = np.repeat(np.arange(M), N)
-    ns = np.tile(np.arange(N), M)
-    yo, ab = oracle.gemm_grouped_points(qao[row_index], sao[:, row_index], qwo, swo, offsets, ms, ns)
-    assert_within_tolerance(bf16_to_f64(y).ravel(), yo, ab, "gather small")
+    assert torch.equal(q, q2) and torch.equal(s.view(torch.int32), s2.view(torch.int32))
+    qo, so = oracle.quant_act_group(x[row_index])
+    assert np.array_equal(q.cpu().numpy(), qo) and np.array_equal(f32_bits(s.cpu().numpy()), f32_bits(so))
 
 
-def test_gather_moe_full_size():
-    """The MoE layer without a permuted copy: X [4096, 7168] quantized in
-    token order, 8 experts [2048, 7168], top-2 routing gathered by the GEMM."""
+def test_gathered_moe_full_size():
+    """The MoE layer without a permuted copy of X: X [4096, 7168] in token
+    order, top-2 routing gathered by the activation quantizer, 8 experts
+    [2048, 7168] in the grouped GEMM; sampled against the oracle."""
     tokens, E, N, K = 4096, 8, 2048, 7168
     x = synth.activations(tokens, K, 0, "moe/X", outlier_channels=0)
     token_of_row, offsets = synth.route_top2(tokens, E, seed=0)
-    qa, sa = ops.quant_act_group(to_dev_bf16(x))
+    M = token_of_row.size
+    qa = torch.empty((M, K), dtype=torch.uint8, device="cuda")
+    sa = torch.empty((K // 128, M), dtype=torch.float32, device="cuda")
+    ops.fp8_quant_act_group_gather(to_dev_bf16(x), torch.from_numpy(token_of_row.astype(np.int32)).cuda(), qa, sa)
     qw = torch.empty((E, N, K), dtype=torch.uint8, device="cuda")
     sw = torch.empty((E, N // 128, K // 128), dtype=torch.float32, device="cuda")
-    ws = [synth.weights(N, K, 0, f"moe/W{e}", sigma=0.02) for e in range(E)]
     for e in range(E):
-        ops.fp8_quant_weight_block(to_dev_bf16(ws[e]), qw[e], sw[e])
-    M = token_of_row.size
+        ops.fp8_quant_weight_block(to_dev_bf16(synth.weights(N, K, 0, f"moe/W{e}", sigma=0.02)), qw[e], sw[e])
     y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-    ops.fp8_block_gemm_gather(qa, sa, torch.from_numpy(token_of_row.astype(np.int32)).cuda(), qw, sw, y,
-                              torch.from_numpy(offsets).cuda())
+    ops.fp8_block_gemm(qa, sa, qw, sw, y, num_groups=E, group_offsets=torch.from_numpy(offsets).cuda())
     assert ops.fp8_device_error() == (0, 0)
+    qao, sao = oracle.quant_act_group(x[token_of_row])
+    assert np.array_equal(qa.cpu().numpy(), qao) and np.array_equal(f32_bits(sa.cpu().numpy()), f32_bits(sao))
     yg = bf16_to_f64(y)
-    qao, sao = oracle.quant_act_group(x)
-    assert np.array_equal(qa.cpu().numpy(), qao)
-    qwo = qw.cpu().numpy()
-    swo = sw.cpu().numpy()
     rng = np.random.default_rng(6)
     edge_rows = np.unique(np.concatenate([offsets[:-1], offsets[1:] - 1]).clip(0, M - 1))
     cols = np.array([0, 127, 128, 1000, N - 1])
     ms = np.concatenate([np.repeat(edge_rows, cols.size), rng.integers(0, M, 4096)])
     ns = np.concatenate([np.tile(cols, edge_rows.size), rng.integers(0, N, 4096)])
-    yo, ab = oracle.gemm_grouped_points(qao[token_of_row], sao[:, token_of_row], qwo, swo, offsets, ms, ns)
+    yo, ab = oracle.gemm_grouped_points(qao, sao, qw.cpu().numpy(), sw.cpu().numpy(), offsets, ms, ns)
     assert_within_tolerance(yg[ms, ns], yo, ab, "gathered moe sampled")
 
 
-def test_gather_bad_row_index_reported():
-    M_src, N, K, E = 64, 128, 256, 2
-    qa = torch.zeros((M_src, K), dtype=torch.uint8, device="cuda")
-    sa = torch.ones((K // 128, M_src), dtype=torch.float32, device="cuda")
-    qw = torch.zeros((E, N, K), dtype=torch.uint8, device="cuda")
-    sw = torch.ones((E, N // 128, K // 128), dtype=torch.float32, device="cuda")
-    off = torch.tensor([0, 20, 40], dtype=torch.int32, device="cuda")
-    y = torch.empty((40, N), dtype=torch.bfloat16, device="cuda")
-    good = torch.arange(40, dtype=torch.int32, device="cuda")
-    ops.fp8_block_gemm_gather(qa, sa, good, qw, sw, y, off)
+def test_quant_gather_bad_row_index_reported():
+    x = synth.device_normal_bf16(64, 256, 0, "gather/bad")
+    ri = torch.arange(40, dtype=torch.int32, device="cuda")
+    q = torch.empty((40, 256), dtype=torch.uint8, device="cuda")
+    s = torch.empty((2, 40), dtype=torch.float32, device="cuda")
+    ops.fp8_quant_act_group_gather(x, ri, q, s)
     assert ops.fp8_device_error() == (0, 0)
-    bad = good.clone()
-    bad[7] = M_src
-    ops.fp8_block_gemm_gather(qa, sa, bad, qw, sw, y, off)
-    assert ops.fp8_device_error() == (5, 107)
+    ri[7] = 64
+    ops.fp8_quant_act_group_gather(x, ri, q, s)
+    assert ops.fp8_device_error() == (5, 303)

@@ -18,7 +18,8 @@ from concurrent.futures import ThreadPoolExecutor
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-PIN_FILES = ["test_oracle_e4m3.py", "test_oracle_quant.py", "test_oracle_gemm.py"]
+PIN_FILES = ["test_oracle_e4m3.py", "test_oracle_quant.py", "test_oracle_gemm.py", "test_oracle_rowwise.py",
+             "test_oracle_kv_cache.py"]
 
 # (name, snippet of fp8_oracle.c, replacement); each snippet occurs exactly once.
 MUTANTS = [
@@ -94,6 +95,20 @@ MUTANTS = [
     ("per-tensor points: weight row of another point", "qa + ms[i] * K, sa, qw + ns[i] * K, sw,",
      "qa + ms[i] * K, sa, qw + ns[npts - 1 - i] * K, sw,"),
     ("grouped: expert 0's weights for every expert", "qw + expert * N * K", "qw"),
+    # BF16 rounding and the FP8 KV cache
+    ("bf16: ties away from zero", "r = nearbyint(a / quantum) * quantum;", "r = round(a / quantum) * quantum;"),
+    ("bf16: seven significant bits", "quantum = ldexp(1.0, exponent - 7);", "quantum = ldexp(1.0, exponent - 6);"),
+    ("bf16: subnormal spacing one binade too fine", "if (exponent < -126)\n        exponent = -126;",
+     "if (exponent < -127)\n        exponent = -127;"),
+    ("kv store: last element of each row skipped",
+     "for (e = 0; e < elems; e++)\n            cache[slots[t] * elems + e]",
+     "for (e = 0; e + 1 < elems; e++)\n            cache[slots[t] * elems + e]"),
+    ("kv store: scale taken as its reciprocal",
+     "cache[slots[t] * elems + e] = quant_value(bf16_bits_to_float(x[t * elems + e]), scale);",
+     "cache[slots[t] * elems + e] = quant_value(bf16_bits_to_float(x[t * elems + e]), 1.0f / scale);"),
+    ("kv load: rows of the mirrored slot", "ora_e4m3_decode(cache[slots[t] * elems + e])",
+     "ora_e4m3_decode(cache[(num_slots - 1 - slots[t]) * elems + e])"),
+    ("kv load: scale ignored", "(double)scale));", "1.0));"),
     ("static quantization: scale taken as its reciprocal",
      "q[i] = quant_value(bf16_bits_to_float(x[i]), scale);",
      "q[i] = quant_value(bf16_bits_to_float(x[i]), 1.0f / scale);"),
