@@ -279,18 +279,8 @@ def run_decode_section(torch, ops, dev, steps, warmup, peaks, sync_ranks):
             qw, sw = layers[layer][i]
             ops.fp8_block_linear(x, qa, sa, qw, sw, ys[layer])
 
-    def step_two_kernels(marks):
-        for (M, layer, i) in calls:
-            N, K = SHAPES[i]
-            x, qa, sa, ys = acts[(M, N, K)]
-            qw, sw = layers[layer][i]
-            ops.fp8_quant_act_group(x, qa, sa)
-            ops.fp8_block_gemm(qa, sa, qw, sw, ys[layer])
-
     step_bytes = sum(linear_bytes(M, *SHAPES[i]) for M, _, i in calls)
     gemm_total_bytes = sum(gemm_bytes(M, *SHAPES[i]) for M, _, i in calls)
-    timed2 = Timed(torch, step_two_kernels)
-    ms2, _ = time_steps(torch, timed2.replay, steps, warmup)
     timed = Timed(torch, step)
     ms, window = time_steps(torch, timed.replay, steps, warmup, sync_ranks)
     value = step_bytes * steps / (ms * 1e-3) / 1e9
@@ -326,10 +316,7 @@ def run_decode_section(torch, ops, dev, steps, warmup, peaks, sync_ranks):
             us = t * 1e3 / (reps * LAYERS)
             per_shape[f"M{M}_N{N}_K{K}"] = {"us": us, "GBps": gemm_bytes(M, N, K) / (us * 1e-6) / 1e9}
     out = {"value": value, "ms_per_step": ms / steps, "roofline": roof, "per_shape": per_shape,
-           "launches_per_step": len(calls), "window": window, "step_bytes": step_bytes,
-           "two_kernel_path": {"value": step_bytes * steps / (ms2 * 1e-3) / 1e9, "ms_per_step": ms2 / steps,
-                               "note": "the same step as fp8_quant_act_group + fp8_block_gemm (a quantizer kernel "
-                                       "and a GEMM kernel per call, chained by programmatic dependent launch)"}}
+           "launches_per_step": 2 * len(calls), "window": window, "step_bytes": step_bytes}
 
     # End to end through the C entry point, as a C caller drives it: the step's
     # 96 activation inputs sit in one pinned host slab and its 96 outputs
@@ -924,7 +911,6 @@ def main():
                          f"({sum(N * K for N, K in SHAPES) * LAYERS / 1e9:.2f} GB) stream once per M per step",
                    "graph": "each step is one CUDA graph replay"},
         "roofline": dec["roofline"], "cpu_baseline": cpu, "e2e": dec["e2e"],
-        "two_kernel_path": dec["two_kernel_path"],
         "gpu_launches": dec["launches_per_step"] * args.steps, "clocks": clocks,
         "decode_per_shape": dec["per_shape"], "sections": sections,
         "device_error": {"code": code, "site": site}, "peaks": peaks,

@@ -204,8 +204,6 @@ int fp8_block_linear(const void *x_bf16, void *qa, float *sa, const void *qw, co
     const fp8k::DeviceInfo *dev = nullptr;
     if (int st = fp8k::current_device(&dev)) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (M <= 16)
-        return fp8k::to_status(fp8k::launch_gemm_decode_fused(x_bf16, qa, sa, qw, sw, y_bf16, M, N, K, *dev, s));
     cudaError_t e = fp8k::launch_quant_act_group(x_bf16, qa, sa, M, K, *dev, s);
     if (e != cudaSuccess) return FP8_ERR_CUDA;
     if (M <= 16) return fp8k::to_status(fp8k::launch_gemm_decode(qa, sa, qw, sw, y_bf16, M, N, K, fp8k::kScaleBlock, *dev, s));

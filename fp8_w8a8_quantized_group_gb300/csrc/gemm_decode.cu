@@ -29,19 +29,6 @@
 //    early); the activation codes and scales are read, and every global
 //    write is made, after griddepcontrol.wait.
 //
-// Fused variant (fp8_block_linear, M <= 16): the 1x128 activation
-// quantization runs inside this kernel, in the operand pipeline. Two warps
-// take each stage's K block of X (BF16, at most 16 rows x 128), quantize it
-// (the same per-group scale and codes as the stand-alone quantizer) and write
-// the codes straight into the stage's shared-memory operand tile in the
-// swizzled layout the MMA reads, and the scales into a small ring the
-// epilogue reads; no code makes a round trip through global memory and no CTA
-// waits for another. Every CTA quantizes the K range it multiplies, so the
-// work is repeated once per 128-row block of weights - cheap here, since it
-// reads X from L2 and uses issue slots the weight stream leaves idle. The CTAs
-// of the first row block also write the codes and scales to qa and sa, so
-// each group is written exactly once.
-//
 // Block mode applies Sw[n/128][kb] * Sa[kb][m] per K block; per-tensor mode
 // accumulates all of the CTA's K range in TMEM and applies sa * sw once;
 // row/column mode does the same with sa[m] * sw[n] (per-token activation and
@@ -66,32 +53,17 @@ constexpr int kL2Warm = 12;     // weight tiles loaded or warmed in L2 before th
 constexpr int kScaleKb = 8;     // K blocks of activation/weight scales staged at a time per epilogue warp
 constexpr int kScaleBytes = 4 * 4 * (kScaleKb * kTok + kScaleKb);
 constexpr int kRecvBytes = kRows * kTok * 4;  // split-K partials addressed to this CTA
-constexpr int kXsRing = 8;     // fused: activation-scale slots, a ring over K blocks (>= kStages + 2)
-constexpr int kQuantBatch = 4; // fused: K blocks of X the quantizer warps load at once
-constexpr int kXsBytes = kXsRing * kTok * 4;
 constexpr int kSmemBytes =
-    1024 + kStages * (kWBytes + kXBytes) + kRecvBytes + 8 * (3 * kStages + 5) + 16 + kScaleBytes + kXsBytes;
-static_assert(kXsRing >= kStages + 2, "a scale slot must outlive the K blocks the MMA runs ahead of the epilogue");
+    1024 + kStages * (kWBytes + kXBytes) + kRecvBytes + 8 * (2 * kStages + 5) + 16 + kScaleBytes;
 
 enum : unsigned { kSiteProdEmpty = 201, kSiteMmaTmem = 202, kSiteMmaFull = 203, kSiteEpiFull = 204,
-                  kSiteDrain = 205, kSiteReduce = 206, kSiteQuantEmpty = 207 };
+                  kSiteDrain = 205, kSiteReduce = 206 };
 
-// Fused activation quantization (block mode only): x is the BF16 input
-// [M][K]; the CTAs of the first row block write the codes to qa_out and the
-// scales to sa_out ([K/128][M]).
-struct FusedQuant {
-    const uint16_t *x;
-    uint8_t *qa_out;
-    float *sa_out;
-};
-
-template <int MODE, bool FUSED>
+template <int MODE>
 __global__ void __launch_bounds__(kThreads, 2)
     gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                        const float *__restrict__ sa, const float *__restrict__ sw,
-                       __nv_bfloat16 *__restrict__ y, int M, int N, int K, int splits, unsigned *err,
-                       FusedQuant fq) {
-    static_assert(!FUSED || MODE == kScaleBlock, "fused activation quantization is block-scaled");
+                       __nv_bfloat16 *__restrict__ y, int M, int N, int K, int splits, unsigned *err) {
     constexpr bool WHOLE_K = MODE != kScaleBlock;  // all of the CTA's K in one TMEM accumulator
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -103,12 +75,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint64_t *tfull = empty + kStages;
     uint64_t *tempty = tfull + 2;
     uint64_t *rbar = tempty + 2;  // completes when all kRecvBytes have arrived
-    uint64_t *xfull = rbar + 1;   // fused: the stage's activation codes are written
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(xfull + kStages);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(rbar + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    volatile int *quant_go = reinterpret_cast<volatile int *>(tmem_slot + 2);  // fused: quantizer's shared decision
     float *scale_smem = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(tmem_slot) + 16);
-    float *xs_ring = scale_smem + kScaleBytes / 4;  // fused: [kXsRing][kTok] activation scales
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nb = blockIdx.x / splits;
@@ -119,9 +88,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int kb1 = static_cast<int>((static_cast<int64_t>(split + 1) * Kg) / splits);
 
     if (threadIdx.x == 0) {
-        // fused: the weights of a stage land on full[s], its activation codes
-        // (written by the quantizer warps) are announced on xfull[s].
-        for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); mbar_init(&xfull[s], 1); }
+        for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
         for (int b = 0; b < 2; ++b) { mbar_init(&tfull[b], 1); mbar_init(&tempty[b], 128); }
         mbar_init(rbar, 1);
         *abort_flag = 0;
@@ -155,24 +122,22 @@ __global__ void __launch_bounds__(kThreads, 2)
             const uint64_t stream_once = policy_evict_first();
             const int nkb = kb1 - kb0;
             const int pre = nkb < kStages ? nkb : kStages;
-            constexpr uint32_t kStageTx = FUSED ? kWBytes : kWBytes + kXBytes;  // fused: X is not loaded by TMA
             for (int i = 0; i < pre; ++i) {
-                mbar_arrive_expect_tx(&full[i], kStageTx);
+                mbar_arrive_expect_tx(&full[i], kWBytes + kXBytes);
                 tma_load_2d_hint(sW + i * kWBytes, &tmW, &full[i], (kb0 + i) * BK, n0, stream_once);
             }
             const int warm = nkb < kL2Warm ? nkb : kL2Warm;
             for (int i = pre; i < warm; ++i) tma_prefetch_l2_2d(&tmW, (kb0 + i) * BK, n0);
             if (splits > 1) cluster_wait_acquire();
             grid_dep_wait();
-            if (!FUSED)
-                for (int i = 0; i < pre; ++i) tma_load_2d(sX + i * kXBytes, &tmX, &full[i], (kb0 + i) * BK, 0);
+            for (int i = 0; i < pre; ++i) tma_load_2d(sX + i * kXBytes, &tmX, &full[i], (kb0 + i) * BK, 0);
             uint32_t stage = static_cast<uint32_t>(pre % kStages), phase = pre == kStages ? 1u : 0u;
             int issued = pre;
             for (int kb = kb0 + pre; kb < kb1; ++kb) {
                 if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err, kSiteProdEmpty)) break;
-                mbar_arrive_expect_tx(&full[stage], kStageTx);
+                mbar_arrive_expect_tx(&full[stage], kWBytes + kXBytes);
                 tma_load_2d_hint(sW + stage * kWBytes, &tmW, &full[stage], kb * BK, n0, stream_once);
-                if (!FUSED) tma_load_2d(sX + stage * kXBytes, &tmX, &full[stage], kb * BK, 0);
+                tma_load_2d(sX + stage * kXBytes, &tmX, &full[stage], kb * BK, 0);
                 ++issued;
                 if (++stage == kStages) { stage = 0; phase ^= 1u; }
             }
@@ -200,7 +165,6 @@ __global__ void __launch_bounds__(kThreads, 2)
                     tc_fence_after();
                 }
                 if (!mbar_wait<true>(&full[stage], phase, abort_flag, err, kSiteMmaFull)) break;
-                if (FUSED && !mbar_wait<true>(&xfull[stage], phase, abort_flag, err, kSiteMmaFull)) break;
                 tc_fence_after();
                 const uint32_t w0 = smem_u32(sW + stage * kWBytes);
                 const uint32_t x0 = smem_u32(sX + stage * kXBytes);
@@ -227,74 +191,6 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
             }
         }
-    } else if (FUSED && (warp == 2 || warp == 3)) {
-        // ------------------------------------------- activation quantizer --
-        // 64 threads per K block: thread t takes token row t/4 and the 16-code
-        // units 2(t%4), 2(t%4)+1 of the block's 8 (16 BF16 each); the row's
-        // amax is reduced over its four threads. The codes go to the stage's
-        // operand tile at the 128-byte-swizzled position the MMA descriptor
-        // reads (unit u of row r at unit u ^ (r % 8)), the scale to the ring.
-        const int t = threadIdx.x - 64;
-        const int row = t >> 2, u0 = (t & 3) * 2;
-        const bool has_row = row < M;
-        const bool writes_out = blockIdx.x < splits;  // the first row block's CTAs write qa and sa
-        grid_dep_wait();
-        uint32_t stage = 0, phase = 0;
-        bool go = true;
-        // X is read kQuantBatch K blocks at a time, all loads in flight
-        // together, so each batch costs one L2 round trip, not one per block.
-        for (int kbb = kb0; kbb < kb1 && go; kbb += kQuantBatch) {
-            uint4 v[kQuantBatch][4];
-#pragma unroll
-            for (int b = 0; b < kQuantBatch; ++b) {
-                const bool ld = has_row && kbb + b < kb1;
-                const uint16_t *src = fq.x + static_cast<int64_t>(row) * K + (kbb + b) * BK + u0 * 16;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) v[b][i] = ld ? ld_stream_v4(src + 8 * i) : make_uint4(0u, 0u, 0u, 0u);
-            }
-#pragma unroll
-            for (int b = 0; b < kQuantBatch; ++b) {
-                const int kb = kbb + b;
-                if (kb >= kb1) break;
-                if (kb - kb0 >= kStages) {
-                    // Thread 0 waits for the stage to be free and decides for
-                    // all 64 (the decision is read after the barrier, and
-                    // rewritten only after the barrier that ends this block).
-                    if (t == 0)
-                        *quant_go = mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err, kSiteQuantEmpty) ? 1 : 0;
-                    named_bar_sync(3, 64);
-                    if (!*quant_go) {
-                        go = false;
-                        break;
-                    }
-                }
-                float a = fmaxf(fmaxf(amax8(v[b][0]), amax8(v[b][1])), fmaxf(amax8(v[b][2]), amax8(v[b][3])));
-                a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-                a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
-                const float sc = block_scale(a);
-                const float rc = __frcp_rn(sc);
-                uint4 c[2];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const uint2 lo = quant8_recip(v[b][2 * h], sc, rc), hi = quant8_recip(v[b][2 * h + 1], sc, rc);
-                    c[h] = has_row ? make_uint4(lo.x, lo.y, hi.x, hi.y) : make_uint4(0u, 0u, 0u, 0u);
-                }
-                uint8_t *tile = sX + stage * kXBytes + row * BK;
-#pragma unroll
-                for (int h = 0; h < 2; ++h) *reinterpret_cast<uint4 *>(tile + (((u0 + h) ^ (row & 7)) << 4)) = c[h];
-                if ((t & 3) == 0) xs_ring[(kb & (kXsRing - 1)) * kTok + row] = has_row ? sc : 0.0f;
-                if (writes_out && has_row) {
-                    uint8_t *dst = fq.qa_out + static_cast<int64_t>(row) * K + kb * BK + u0 * 16;
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) *reinterpret_cast<uint4 *>(dst + 16 * h) = c[h];
-                    if ((t & 3) == 0) fq.sa_out[static_cast<int64_t>(kb) * M + row] = sc;
-                }
-                fence_proxy_async_smem();  // the MMA (async proxy) reads these shared-memory writes
-                named_bar_sync(3, 64);
-                if (t == 0) mbar_arrive(&xfull[stage]);
-                if (++stage == kStages) { stage = 0; phase ^= 1u; }
-            }
-        }
     } else if (warp >= 4) {
         // ---------------------------------------------------------- epilogue --
         const int ep = warp - 4;
@@ -315,8 +211,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                 for (int i = 0; i < kScaleKb * kTok / 32; ++i) {
                     const int idx = lane + 32 * i;
-                    // (fused: the activation scales come from the ring instead)
-                    r_sa[i] = (!FUSED && idx < n * M) ? __ldg(sa + static_cast<int64_t>(c0) * M + idx) : 0.0f;
+                    r_sa[i] = idx < n * M ? __ldg(sa + static_cast<int64_t>(c0) * M + idx) : 0.0f;
                 }
                 r_sw = lane < n ? __ldg(swrow + c0 + lane) : 0.0f;
             };
@@ -332,17 +227,12 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const int c1 = min(kb1, c0 + kScaleKb);
                 for (int kb = c0; kb < c1; ++kb) {
                     const float wscale = w_sw[kb - c0];
+                    const float *srow = w_sa + (kb - c0) * M;
                     if (!__all_sync(0xffffffffu, mbar_wait(&tfull[buf], bphase, abort_flag, err, kSiteEpiFull))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    // fused: the K block's MMA is complete, so its scales are in
-                    // the ring (written before the stage was marked full), and
-                    // the slot is not rewritten before this block's TMEM buffer
-                    // is released (the quantizer runs at most kStages + 1 K
-                    // blocks ahead of that).
-                    const float *srow = FUSED ? xs_ring + (kb & (kXsRing - 1)) * kTok : w_sa + (kb - c0) * M;
                     float p[kTok];
                     tmem_ld16(lane_addr + buf * kTok, p);
                     tc_fence_before();
@@ -464,40 +354,30 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 }
 
-// Split of K over a cluster: as far as all CTAs still fit on the GPU at once
-// (two per SM), so that no CTA waits for a second wave.
-int pick_splits(int64_t N, int64_t K, const DeviceInfo &dev) {
-    const int64_t nblocks = (N + kRows - 1) / kRows;
-    const int64_t Kg = (K + BK - 1) / BK;
-    int splits = 1;
-    while (splits < 8 && nblocks * splits * 2 <= 2 * dev.sm_count && splits * 2 <= Kg) splits *= 2;
-    return splits;
-}
-
-template <int MODE, bool FUSED>
-cudaError_t set_attributes() {
+template <int MODE>
+cudaError_t launch_variant(const void *qa, const float *sa, const void *qw, const float *sw, void *y, int64_t M,
+                           int64_t N, int64_t K, const DeviceInfo &dev, cudaStream_t stream) {
     static std::once_flag attr_once[64];
     static cudaError_t attr_err[64];
     int device = 0;
     cudaGetDevice(&device);
     std::call_once(attr_once[device & 63], [&] {
-        attr_err[device & 63] = cudaFuncSetAttribute(gemm_decode_kernel<MODE, FUSED>,
-                                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(gemm_decode_kernel<MODE>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        attr_err[device & 63] = e;
     });
-    return attr_err[device & 63];
-}
+    if (attr_err[device & 63] != cudaSuccess) return attr_err[device & 63];
 
-template <int MODE, bool FUSED = false>
-cudaError_t launch_variant(const void *qa, const float *sa, const void *qw, const float *sw, void *y, int64_t M,
-                           int64_t N, int64_t K, const DeviceInfo &dev, cudaStream_t stream,
-                           FusedQuant fq = FusedQuant{nullptr, nullptr, nullptr}) {
-    if (cudaError_t e = set_attributes<MODE, FUSED>()) return e;
     CUtensorMap tmW, tmX;
     if (encode_tma_2d_u8(&tmW, qw, K, N, K, BK, kRows) != CUDA_SUCCESS) return cudaErrorInvalidValue;
     if (encode_tma_2d_u8(&tmX, qa, K, M, K, BK, kTok) != CUDA_SUCCESS) return cudaErrorInvalidValue;
 
     const int64_t nblocks = (N + kRows - 1) / kRows;
-    const int splits = pick_splits(N, K, dev);
+    const int64_t Kg = (K + BK - 1) / BK;
+    // Split K over a cluster as far as all CTAs still fit on the GPU at once
+    // (two per SM), so that no CTA waits for a second wave.
+    int splits = 1;
+    while (splits < 8 && nblocks * splits * 2 <= 2 * dev.sm_count && splits * 2 <= Kg) splits *= 2;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(nblocks * splits));
@@ -513,9 +393,9 @@ cudaError_t launch_variant(const void *qa, const float *sa, const void *qw, cons
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, gemm_decode_kernel<MODE, FUSED>, tmW, tmX, sa, sw,
+    return cudaLaunchKernelEx(&cfg, gemm_decode_kernel<MODE>, tmW, tmX, sa, sw,
                               static_cast<__nv_bfloat16 *>(y), static_cast<int>(M), static_cast<int>(N),
-                              static_cast<int>(K), splits, dev.err, fq);
+                              static_cast<int>(K), splits, dev.err);
 }
 
 }  // namespace
@@ -526,12 +406,6 @@ cudaError_t launch_gemm_decode(const void *qa, const float *sa, const void *qw, 
     if (mode == kScaleTensor) return launch_variant<kScaleTensor>(qa, sa, qw, sw, y, M, N, K, dev, stream);
     if (mode == kScaleRowCol) return launch_variant<kScaleRowCol>(qa, sa, qw, sw, y, M, N, K, dev, stream);
     return launch_variant<kScaleBlock>(qa, sa, qw, sw, y, M, N, K, dev, stream);
-}
-
-cudaError_t launch_gemm_decode_fused(const void *x, void *qa, float *sa, const void *qw, const float *sw, void *y,
-                                     int64_t M, int64_t N, int64_t K, const DeviceInfo &dev, cudaStream_t stream) {
-    const FusedQuant fq{static_cast<const uint16_t *>(x), static_cast<uint8_t *>(qa), sa};
-    return launch_variant<kScaleBlock, true>(qa, sa, qw, sw, y, M, N, K, dev, stream, fq);
 }
 
 }  // namespace fp8k

@@ -59,12 +59,6 @@ cudaError_t launch_gemm_decode(const void *qa, const float *sa, const void *qw, 
                                int64_t M, int64_t N, int64_t K, ScaleMode mode, const DeviceInfo &dev,
                                cudaStream_t stream);
 
-// The decode GEMM with the 1x128 activation quantization fused in (M <= 16,
-// block mode): two warps of every CTA quantize each K block of x into the
-// shared-memory operand stage; the first row block's CTAs also write qa / sa.
-cudaError_t launch_gemm_decode_fused(const void *x, void *qa, float *sa, const void *qw, const float *sw, void *y,
-                                     int64_t M, int64_t N, int64_t K, const DeviceInfo &dev, cudaStream_t stream);
-
 // One CTA whose waits never complete: the first gives up after the wait limit
 // and records FP8_ERR_TIMEOUT (site 901); the second returns at the abort flag.
 cudaError_t launch_selftest_wait(const DeviceInfo &dev, cudaStream_t stream);

@@ -79,6 +79,40 @@ __global__ void __launch_bounds__(kActThreads, 6) quant_act_group_kernel(const u
                         [](const uint16_t *p) { return ld_stream_v4(p); });
 }
 
+// Decode-sized inputs (few rows): the kernel above gives each lane 32
+// elements and puts only a few CTAs on the GPU, so a call is bound by one
+// lane's dependent chain. Here each lane takes one 16-byte chunk (8 elements)
+// and a group is spread over 16 lanes (two groups per warp, 16 per CTA), and
+// the codes take the reciprocal route (quant8_recip, the same codes as the
+// division). CTA b covers groups 16b .. 16b+15 in (row, group) order.
+constexpr int kActSmallThreads = 256;
+constexpr int64_t kActSmallMaxRows = 16;  // the decode sizes; larger M takes the kernel above
+constexpr int kActSmallGroups = kActSmallThreads / 16;
+
+__global__ void __launch_bounds__(kActSmallThreads) quant_act_group_small_kernel(const uint16_t *__restrict__ x,
+                                                                                uint8_t *__restrict__ q,
+                                                                                float *__restrict__ s, int M,
+                                                                                int Kg) {
+    const int lane = threadIdx.x & 31;
+    const int c = lane & 15;
+    const int gi = blockIdx.x * kActSmallGroups + (threadIdx.x >> 4);
+    const bool ok = gi < M * Kg;
+    const int m = ok ? gi / Kg : 0;
+    const int g = ok ? gi - m * Kg : 0;
+    grid_dep_launch();
+    grid_dep_wait();
+    const int64_t off = static_cast<int64_t>(m) * Kg * 128 + g * 128 + c * 8;
+    const uint4 v = ok ? ld_stream_v4(x + off) : make_uint4(0u, 0u, 0u, 0u);
+    float a = amax8(v);
+#pragma unroll
+    for (int o = 1; o < 16; o <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    if (ok) {
+        const float sc = block_scale(a);
+        *reinterpret_cast<uint2 *>(q + off) = quant8_recip(v, sc, __frcp_rn(sc));
+        if (c == 0) s[static_cast<int64_t>(g) * M + m] = sc;
+    }
+}
+
 // --------------------------------------------------- 128 x 128 weight blocks --
 
 constexpr int kWThreads = 256;
@@ -326,6 +360,20 @@ cudaError_t launch_quant_rows(const void *x, void *q, float *s, int64_t rows, in
 cudaError_t launch_quant_act_group(const void *x, void *q, float *s, int64_t M, int64_t K,
                                    const DeviceInfo &dev, cudaStream_t stream, const int32_t *row_index,
                                    int64_t M_src) {
+    const int64_t groups = M * (K / 128);
+    if (row_index == nullptr && M <= kActSmallMaxRows && groups > 0) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>((groups + kActSmallGroups - 1) / kActSmallGroups));
+        cfg.blockDim = dim3(kActSmallThreads);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, quant_act_group_small_kernel, static_cast<const uint16_t *>(x),
+                                  static_cast<uint8_t *>(q), s, static_cast<int>(M), static_cast<int>(K / 128));
+    }
     const int64_t rows = (M + kActRows - 1) / kActRows;
     const int64_t cols = (K / 128 + kActGroups - 1) / kActGroups;
     if (rows == 0 || cols == 0) return cudaSuccess;

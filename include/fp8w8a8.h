@@ -66,9 +66,9 @@
  *    decode GEMM             lets its dependent launch early; it writes y
  *                            after its own wait, and reads only qw early;
  *    prefill GEMM            does not;
- *    fp8_block_linear        M <= 16: one kernel, as the decode GEMM; M > 16:
- *                            its quantizer lets the prefill GEMM launch early
- *                            (that GEMM does not read before its wait).
+ *    fp8_block_linear        its quantizer lets its own GEMM launch early (the
+ *                            GEMM reads qa and sa after its wait); its GEMM is
+ *                            the decode or prefill GEMM above.
  * Work that is not this library's (torch kernels, copies) never triggers
  * early, so a plain stream order with it is always safe.
  */
@@ -316,16 +316,11 @@ int fp8_kv_cache_load(const void *key_cache, const void *value_cache, void *key_
  *   y       [M][N] BF16, output.
  *   K a positive multiple of 128 up to FP8_ACT_GROUP_MAX_K, N a positive
  *   multiple of 16, M >= 0.
- * M <= 16 (decode): ONE launch. The activation quantization runs inside the
- * decode GEMM kernel: two warps of every CTA quantize each K block of X into
- * the shared-memory operand stage the MMA reads (the quantize/dequantize
- * overhead of "FP8 Quantization", section E, item 4, kept off the critical
- * path: no separate kernel, no round trip of the codes through memory, no
- * grid-wide wait). The CTAs of the first 128-row weight block also write qa
- * and sa, each group exactly once.
- * M > 16 (prefill): two launches, the quantization kernel then the prefill
- * GEMM; the quantization kernel is a programmatic dependent of the work
- * before it.
+ * Two launches on `stream`: the quantization kernel, then the decode
+ * (M <= 16) or prefill GEMM. The quantization kernel is a programmatic
+ * dependent of the work before it, and the GEMM of the quantization kernel:
+ * each starts its prologue (and the decode GEMM loads its first weights)
+ * while its predecessor finishes, and waits for it before reading its output.
  * Errors: NULL, SHAPE, ALIGN, DEVICE, CUDA.
  */
 int fp8_block_linear(const void *x_bf16, void *qa, float *sa, const void *qw, const float *sw,

@@ -347,16 +347,16 @@ def test_rowwise_gemm_full_size(M, N, K):
     assert_within_tolerance(yg[ms, ns], yo, ab, f"rowwise {M}x{N}x{K} sampled")
 
 
-# ---------------------------------- activation quantization in the GEMM --
+# ------------------------------------------- the linear layer at decode --
 
 @pytest.mark.parametrize("M,N,K", [(16, 4096, 4096), (16, 6144, 4096), (16, 4096, 14336), (9, 1024, 1280),
                                    (2, 19584, 8320), (16, 256, 128)])
-def test_block_linear_decode_is_one_kernel_matching_separate_calls(M, N, K):
-    """At M <= 16 fp8_block_linear quantizes inside the decode GEMM (two warps
-    fill each stage's operand tile; the first row block's CTAs write qa and
-    sa). Codes, scales and Y are bit-identical to fp8_quant_act_group followed
-    by fp8_block_gemm, here for K ranges of one to 65 blocks per CTA, split
-    and unsplit, and M not a multiple of four."""
+def test_block_linear_decode_matches_separate_calls(M, N, K):
+    """At decode sizes fp8_block_linear (the quantizer chained to the decode
+    GEMM by programmatic dependent launch) writes codes, scales and Y
+    bit-identical to fp8_quant_act_group followed by fp8_block_gemm, for K
+    ranges of one to 65 blocks per CTA, split and unsplit, and M not a
+    multiple of four."""
     xd = synth.device_normal_bf16(M, K, 21, f"fused/X/{M}x{K}", outlier_cols=[3, K // 2], outlier_scale=50.0)
     wd = synth.device_normal_bf16(N, K, 21, f"fused/W/{N}x{K}", sigma=0.02)
     qw, sw = ops.quant_weight_block(wd)
@@ -380,7 +380,7 @@ def test_block_linear_decode_is_one_kernel_matching_separate_calls(M, N, K):
 
 
 def test_block_linear_back_to_back_no_sync():
-    """Twenty one-kernel linear calls on one stream, fresh activations, one
+    """Twenty linear calls on one stream, fresh activations, one
     shared qa / sa pair (as a layer loop reuses them), no host sync: each Y
     matches the two-kernel path bit for bit."""
     M, N, K = 16, 4096, 4096

@@ -34,9 +34,10 @@ def test_act_group_bit_exact(M, K):
     assert np.array_equal(q.cpu().numpy(), qo)
 
 
-def test_act_group_special_values():
+@pytest.mark.parametrize("M", [24, 6])  # the general and the decode-sized kernel
+def test_act_group_special_values(M):
     rng = np.random.default_rng(3)
-    M, K = 24, 512
+    K = 512
     x = synth.to_bf16(rng.standard_normal((M, K)))
     x[0, :] = 0                       # all-zero row: floor scale, +0 codes
     x[1, :128] = 0x8000               # -0.0 group
