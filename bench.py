@@ -43,6 +43,9 @@ import synth  # noqa: E402
 SHAPES = synth.LLAMA8B_SHAPES
 DECODE_M = synth.DECODE_M
 LAYERS = 8
+SUSTAINED_S = 2.0  # seconds of replays in the sustained leg of the headline
+CPU_SAMPLE_S = 8.0  # seconds of oracle work in each cpu_baseline leg (all cores, one core)
+REF_TOTAL_S = 90.0  # target length of a whole --impl reference run
 METRIC = "FP8 block-scaled GEMM TFLOPS (% FP8 peak); decode-M HBM GB/s (% of peak)"
 FP8_OVER_BF16 = 2.0  # nominal dense FP8 / BF16 tensor throughput ratio
 
@@ -284,6 +287,14 @@ def run_decode_section(torch, ops, dev, steps, warmup, peaks, sync_ranks):
     timed = Timed(torch, step)
     ms, window = time_steps(torch, timed.replay, steps, warmup, sync_ranks)
     value = step_bytes * steps / (ms * 1e-3) / 1e9
+    # Sustained: the same step replayed for at least SUSTAINED_S seconds
+    # (whatever --steps is), so that the clocks are sampled under a long load.
+    sus = None
+    if SUSTAINED_S > 0:
+        n_sus = max(steps, int(SUSTAINED_S / max(ms / steps * 1e-3, 1e-6)) + 1)
+        ms_sus, window_sus = time_steps(torch, timed.replay, n_sus, 1, sync_ranks)
+        sus = {"value": step_bytes * n_sus / (ms_sus * 1e-3) / 1e9, "unit": "GB/s", "steps": n_sus,
+               "seconds": ms_sus * 1e-3, "ms_per_step": ms_sus / n_sus, "window": window_sus}
 
     # Dominant kernel: the same GEMM launches back to back in one graph (the
     # activation codes are already in place), timed with events around the
@@ -316,7 +327,7 @@ def run_decode_section(torch, ops, dev, steps, warmup, peaks, sync_ranks):
             us = t * 1e3 / (reps * LAYERS)
             per_shape[f"M{M}_N{N}_K{K}"] = {"us": us, "GBps": gemm_bytes(M, N, K) / (us * 1e-6) / 1e9}
     out = {"value": value, "ms_per_step": ms / steps, "roofline": roof, "per_shape": per_shape,
-           "launches_per_step": 2 * len(calls), "window": window, "step_bytes": step_bytes}
+           "launches_per_step": 2 * len(calls), "window": window, "step_bytes": step_bytes, "sustained": sus}
 
     # End to end through the C entry point, as a C caller drives it: the step's
     # 96 activation inputs sit in one pinned host slab and its 96 outputs
@@ -421,15 +432,61 @@ def run_prefill_section(torch, ops, dev, steps, warmup, peaks):
 
 
 def run_tensor_section(torch, ops, dev, steps, warmup, peaks):
+    """Per-tensor W8A8 layer, N = K = 8192, static weight scale, dynamic
+    activation scale. M <= 16 is timed as the headline is: 8 layers of
+    distinct weights (512 MB, far beyond L2) back to back in one graph, each
+    call the per-tensor quantization of X chained to the decode GEMM; GB/s of
+    the GEMM's algorithmic bytes over the GEMM launches alone, and of the
+    whole layer. M >= 512 is timed per GEMM after a 256 MB L2 flush
+    (TFLOP/s against the FP8 peak)."""
     N = K = 8192
-    w = synth.device_normal_bf16(N, K, 0, "bench/Wt", sigma=0.015,
-                                 outlier_rows=synth.pick(0, "bench/Wt/rows", N, 8), outlier_scale=20.0, device=dev)
-    qw, sw = ops.quant_per_tensor(w)          # load time: dynamic scale of W becomes its static scale
-    qw, sw = ops.quant_per_tensor(w, scale=sw)
-    del w
+    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+    layers = []
+    for layer in range(LAYERS):
+        w = synth.device_normal_bf16(N, K, layer, "bench/Wt", sigma=0.015,
+                                     outlier_rows=synth.pick(0, "bench/Wt/rows", N, 8), outlier_scale=20.0,
+                                     device=dev)
+        qw, sw = ops.quant_per_tensor(w)          # load time: dynamic scale of W becomes its static scale
+        qw, sw = ops.quant_per_tensor(w, scale=sw)
+        layers.append((qw, sw))
+        del w
+    out = {"per_shape": {}}
+    cols = synth.pick(0, f"bench/Xt/outliers/{K}", K, int(round(0.001 * K)))
+    for M in [m for m in synth.PER_TENSOR_M if m <= 16]:
+        x = synth.device_normal_bf16(M, K, 0, f"bench/Xt/{M}", outlier_cols=cols, outlier_scale=100.0, device=dev)
+        qa = torch.empty((M, K), dtype=torch.uint8, device=dev)
+        sa = torch.empty(1, dtype=torch.float32, device=dev)
+        ys = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _ in range(LAYERS)]
+        ops.fp8_quant_per_tensor(x, qa, sa, False)
+
+        def gemms(marks, qa=qa, sa=sa, ys=ys):
+            for layer, (qw, sw) in enumerate(layers):
+                ops.fp8_tensor_gemm(qa, sa, qw, sw, ys[layer])
+
+        def layer_calls(marks, x=x, qa=qa, sa=sa, ys=ys):
+            for layer, (qw, sw) in enumerate(layers):
+                ops.fp8_quant_per_tensor(x, qa, sa, False)
+                ops.fp8_tensor_gemm(qa, sa, qw, sw, ys[layer])
+        reps = max(5, steps)
+        g = Timed(torch, gemms)
+        ms_g, _ = time_steps(torch, g.replay, reps, warmup)
+        g2 = Timed(torch, layer_calls)
+        ms_l, _ = time_steps(torch, g2.replay, reps, warmup)
+        us = ms_g * 1e3 / (reps * LAYERS)
+        us_l = ms_l * 1e3 / (reps * LAYERS)
+        nbytes = tensor_gemm_bytes(M, N, K)
+        lbytes = nbytes + 2 * M * K + 2 * M * K  # + the activations, read twice by the dynamic per-tensor pass
+        out["per_shape"][f"M{M}"] = {
+            "us": us, "GBps": nbytes / (us * 1e-6) / 1e9,
+            "roofline": {"bound": "hbm", "achieved": nbytes / (us * 1e-6) / 1e9, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": nbytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"],
+                         "peak_source": f"hbm_gbs of {peaks['source']}"},
+            "layer_us": us_l, "layer_GBps": lbytes / (us_l * 1e-6) / 1e9,
+            "timing": "8 distinct 64 MB weights back to back in a graph; layer = dynamic per-tensor "
+                      "quantization of X + the GEMM"}
+    qw, sw = layers[0]
     calls = []
-    for M in synth.PER_TENSOR_M:
-        cols = synth.pick(0, f"bench/Xt/outliers/{K}", K, int(round(0.001 * K)))
+    for M in [m for m in synth.PER_TENSOR_M if m > 16]:
         x = synth.device_normal_bf16(M, K, 0, f"bench/Xt/{M}", outlier_cols=cols, outlier_scale=100.0, device=dev)
         qa = torch.empty((M, K), dtype=torch.uint8, device=dev)
         sa = torch.empty(1, dtype=torch.float32, device=dev)
@@ -449,13 +506,19 @@ def run_tensor_section(torch, ops, dev, steps, warmup, peaks):
 
     timed = Timed(torch, step, n_marks=len(calls))
     time_steps(torch, timed.replay, steps, warmup)
-    per = {}
     if timed.ext:
         for j, (M, *_r) in enumerate(calls):
             t = timed.mark_ms()[j] * 1e-3
-            per[f"M{M}"] = {"us": t * 1e6, "TFLOPS": 2.0 * M * N * K / t / 1e12,
-                            "GBps": tensor_gemm_bytes(M, N, K) / t / 1e9}
-    return {"per_shape": per, "note": "M <= 16 is HBM-bound (GB/s), M >= 512 tensor-bound (TFLOPS)"}
+            tf = 2.0 * M * N * K / t / 1e12
+            out["per_shape"][f"M{M}"] = {
+                "us": t * 1e6, "TFLOPS": tf, "GBps": tensor_gemm_bytes(M, N, K) / t / 1e9,
+                "roofline": {"bound": "tensor", "achieved": tf, "peak": fp8_peak, "unit": "TFLOP/s",
+                             "frac": tf / fp8_peak,
+                             "peak_source": f"bf16_tflops of {peaks['source']} x {FP8_OVER_BF16}"},
+                "timing": "the GEMM alone after a 256 MB L2 flush"}
+    out["note"] = "M <= 16 is HBM-bound (GB/s), M >= 512 tensor-bound (TFLOPS)"
+    del layers, calls, flush
+    return out
 
 
 def run_moe_section(torch, ops, dev, steps, warmup, peaks):
@@ -621,35 +684,42 @@ def run_rowwise_section(torch, ops, dev, steps, warmup, peaks):
 
 
 def run_kv_section(torch, ops, dev, steps, warmup, peaks):
-    """FP8 KV cache: store one prefill batch of 8192 tokens (8 KV heads x 128,
+    """FP8 KV cache: store prefill batches of 8192 tokens (8 KV heads x 128,
     keys and values) into random slots of a 65536-slot cache, and gather-load
-    all 65536 slots back to BF16. HBM GB/s of algorithmic bytes."""
-    T, E, S = 8192, 1024, 65536
-    k = synth.device_normal_bf16(T, E, 0, "bench/kv/k", device=dev)
-    v = synth.device_normal_bf16(T, E, 0, "bench/kv/v", device=dev)
+    all 65536 slots back to BF16. HBM GB/s of algorithmic bytes. The stores
+    are timed as four distinct batches back to back in one graph (134 MB of
+    inputs, more than L2), per store."""
+    T, E, S, B = 8192, 1024, 65536, 4
+    ks_in = [synth.device_normal_bf16(T, E, b, "bench/kv/k", device=dev) for b in range(B)]
+    vs_in = [synth.device_normal_bf16(T, E, b, "bench/kv/v", device=dev) for b in range(B)]
     kc = torch.zeros((S, E), dtype=torch.uint8, device=dev)
     vc = torch.zeros((S, E), dtype=torch.uint8, device=dev)
     g = torch.Generator(device=dev)
     g.manual_seed(5)
-    slots = torch.randperm(S, generator=g, device=dev)[:T].contiguous()
+    perm = torch.randperm(S, generator=g, device=dev)
+    slot_sets = [perm[b * T:(b + 1) * T].contiguous() for b in range(B)]
     all_slots = torch.randperm(S, generator=g, device=dev).contiguous()
     ks = torch.tensor([0.02], dtype=torch.float32, device=dev)
     vs = torch.tensor([0.015], dtype=torch.float32, device=dev)
     ko = torch.empty((S, E), dtype=torch.bfloat16, device=dev)
     vo = torch.empty((S, E), dtype=torch.bfloat16, device=dev)
     out = {}
-    jobs = [("store 8192 tokens", lambda: ops.fp8_kv_cache_store(k, v, kc, vc, slots, ks, vs),
-             2 * T * E * 3 + 8 * T),
-            ("load 65536 slots", lambda: ops.fp8_kv_cache_load(kc, vc, ko, vo, all_slots, ks, vs),
+    def stores():
+        for b in range(B):
+            ops.fp8_kv_cache_store(ks_in[b], vs_in[b], kc, vc, slot_sets[b], ks, vs)
+
+    jobs = [("store 8192 tokens", stores, B, 2 * T * E * 3 + 8 * T),
+            ("load 65536 slots", lambda: ops.fp8_kv_cache_load(kc, vc, ko, vo, all_slots, ks, vs), 1,
              2 * S * E * 3 + 8 * S)]
-    for name, fn, nbytes in jobs:
+    for name, fn, calls, nbytes in jobs:
         timed = Timed(torch, lambda marks, fn=fn: fn())
         ms, _ = time_steps(torch, timed.replay, steps, warmup)
-        t = ms / steps * 1e-3
+        t = ms / steps / calls * 1e-3
         out[name] = {"us": t * 1e6, "GBps": nbytes / t / 1e9, "frac_hbm": nbytes / t / 1e9 / peaks["hbm_gbs"]}
     out["note"] = ("E = 8 KV heads x 128; store reads BF16 K and V and writes E4M3 codes (3 B per element each), "
-                   "load reads codes and writes BF16; inputs of 33.6 / 134 MB vs the 129 MB L2")
-    del k, v, kc, vc, ko, vo
+                   "timed per store over 4 distinct 8192-token batches in one graph (134 MB of inputs); load reads "
+                   "codes and writes BF16 (134 MB of codes); both larger than the 129 MB L2")
+    del ks_in, vs_in, kc, vc, ko, vo
     return out
 
 
@@ -668,13 +738,14 @@ def _cpu_weights(N, K, n):
     return _CPU_WEIGHTS[key]
 
 
-def oracle_decode_sample(threads: int | None = None, ms=None, cols: int | None = None):
+def oracle_decode_sample(threads: int | None = None, ms=None, cols: int | None = None, min_seconds: float = 0.0):
     """Times the CPU oracle on one layer of the decode workload: for each M in
     `ms` and each projection, activation quantization of X [M, K] and the FP64
     dequantize-then-GEMM over the first `cols` output columns (all N by
     default). `threads` host threads split the output columns at 128-column
-    boundaries (the oracle's C calls release the GIL). Returns (GB/s of
-    algorithmic bytes, description, seconds)."""
+    boundaries (the oracle's C calls release the GIL). The layer is repeated
+    until the timed total reaches `min_seconds` (at least once). Returns (GB/s
+    of algorithmic bytes, description, seconds)."""
     import concurrent.futures as cf
 
     import oracle
@@ -683,24 +754,28 @@ def oracle_decode_sample(threads: int | None = None, ms=None, cols: int | None =
     ms = list(ms or DECODE_M)
     cases = [(N, K, min(N, cols) if cols else N) for (N, K) in SHAPES]
     xs = {(M, K): synth.activations(M, K, 0, f"cpu/X/{M}x{K}") for M in ms for (_, K, _) in cases}
-    t_total, nbytes = 0.0, 0.0
+    t_total, nbytes, passes = 0.0, 0.0, 0
     with cf.ThreadPoolExecutor(max_workers=threads) as ex:
-        for M in ms:
-            for (N, K, n) in cases:
-                qw, sw = _cpu_weights(N, K, n)
-                blocks = -(-n // 128)
-                bounds = [128 * (blocks * i // threads) for i in range(threads + 1)]
-                bounds[-1] = n
-                t0 = time.perf_counter()
-                qa, sa = oracle.quant_act_group(xs[(M, K)])
-                futs = [ex.submit(oracle.gemm_block, qa, sa, qw[a:b], sw[a // 128:-(-b // 128)], with_absdot=False)
-                        for a, b in zip(bounds[:-1], bounds[1:]) if b > a]
-                for f in futs:
-                    f.result()
-                t_total += time.perf_counter() - t0
-                nbytes += linear_bytes(M, n, K)
+        while passes == 0 or t_total < min_seconds:
+            for M in ms:
+                for (N, K, n) in cases:
+                    qw, sw = _cpu_weights(N, K, n)
+                    blocks = -(-n // 128)
+                    bounds = [128 * (blocks * i // threads) for i in range(threads + 1)]
+                    bounds[-1] = n
+                    t0 = time.perf_counter()
+                    qa, sa = oracle.quant_act_group(xs[(M, K)])
+                    futs = [ex.submit(oracle.gemm_block, qa, sa, qw[a:b], sw[a // 128:-(-b // 128)],
+                                      with_absdot=False)
+                            for a, b in zip(bounds[:-1], bounds[1:]) if b > a]
+                    for f in futs:
+                        f.result()
+                    t_total += time.perf_counter() - t0
+                    nbytes += linear_bytes(M, n, K)
+            passes += 1
     desc = (f"one layer of the decode step: M in {ms} x the four projections, activation quantization + FP64 GEMM "
-            f"on the first {[n for (_, _, n) in cases]} output columns, C oracle on {threads} host thread(s)")
+            f"on the first {[n for (_, _, n) in cases]} output columns, C oracle on {threads} host thread(s)"
+            + (f", {passes} passes" if passes > 1 else ""))
     return nbytes / t_total / 1e9, desc, t_total
 
 
@@ -733,8 +808,15 @@ def reference_arm(args):
     vals = []
     desc = ""
     threads = os.cpu_count() or 1
+    # Size each step so that the whole run takes about REF_TOTAL_S: time a
+    # 512-column slice of the layer once (untimed calibration), then scale the
+    # columns (whole 128-column blocks, at most all of N).
+    _, _, t512 = oracle_decode_sample(threads, cols=512)
+    per_step = REF_TOTAL_S / max(1, args.warmup + args.steps)
+    cols = max(128, int(512 * per_step / max(t512, 1e-6)) // 128 * 128)
+    cols = None if cols >= max(N for N, _ in SHAPES) else cols
     for i in range(args.warmup + args.steps):
-        v, desc, _ = oracle_decode_sample(threads)
+        v, desc, _ = oracle_decode_sample(threads, cols=cols)
         if i >= args.warmup:
             vals.append(v)
     value = statistics.median(vals)
@@ -754,7 +836,9 @@ def reference_arm(args):
 
 def run_case(spec: str, launches: int):
     """One kernel on one shape, for profiling: KIND:M:N:K with KIND in
-    decode|prefill|linear|tensor|moe|act|weight|ptensor. Prints per-launch times."""
+    decode|prefill|linear|tensor|rowwise|moe|act|weight|ptensor|kvstore|kvload (for the KV
+    kinds M is the tokens, K the elements per token, N the cache slots). Prints
+    per-launch times."""
     import torch
 
     import __graft_entry__
@@ -794,6 +878,24 @@ def run_case(spec: str, launches: int):
         y = torch.empty((xp.shape[0], N), dtype=torch.bfloat16, device=dev)
         offd = torch.from_numpy(off).to(dev)
         fn = lambda: ops.fp8_block_gemm(qa, sa, qw, sw, y, num_groups=E, group_offsets=offd)  # noqa: E731
+    elif kind == "rowwise":
+        qa, sa = ops.quant_rowwise(x)
+        qw, sw = ops.quant_rowwise(synth.device_normal_bf16(N, K, 0, "case/W", sigma=0.02, device=dev))
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        fn = lambda: ops.fp8_rowwise_gemm(qa, sa, qw, sw, y)  # noqa: E731
+    elif kind in ("kvstore", "kvload"):
+        # M tokens of K elements each, N cache slots (a random permutation)
+        kc = torch.zeros((N, K), dtype=torch.uint8, device=dev)
+        vc = torch.zeros((N, K), dtype=torch.uint8, device=dev)
+        g = torch.Generator(device=dev)
+        g.manual_seed(5)
+        sl = torch.randperm(N, generator=g, device=dev)[:M].contiguous()
+        ks = torch.tensor([0.02], dtype=torch.float32, device=dev)
+        xo = torch.empty_like(x)
+        if kind == "kvstore":
+            fn = lambda: ops.fp8_kv_cache_store(x, x, kc, vc, sl, ks, ks)  # noqa: E731
+        else:
+            fn = lambda: ops.fp8_kv_cache_load(kc, vc, x, xo, sl, ks, ks)  # noqa: E731
     elif kind == "act":
         qa = torch.empty((M, K), dtype=torch.uint8, device=dev)
         sa = torch.empty((K // 128, M), dtype=torch.float32, device=dev)
@@ -831,6 +933,7 @@ def run_case(spec: str, launches: int):
 # ------------------------------------------------------------------- main --
 
 def main():
+    global SUSTAINED_S
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
@@ -839,11 +942,14 @@ def main():
     ap.add_argument("--sections", default="prefill,tensor,moe,quant,rowwise,kv")
     ap.add_argument("--case", default=None, help="profile one kernel: KIND:M:N:K")
     ap.add_argument("--launches", type=int, default=3)
+    ap.add_argument("--sustained", type=float, default=SUSTAINED_S,
+                    help="seconds of replays in the sustained leg of the headline (0: skip it)")
     args = ap.parse_args()
     if args.case:
         run_case(args.case, args.launches)
         return
     args.warmup = max(3, args.warmup)
+    SUSTAINED_S = args.sustained
     if args.impl == "reference":
         reference_arm(args)
         return
@@ -884,6 +990,8 @@ def main():
     finally:
         sampler.stop()
     clocks = sampler.summary(*dec["window"])
+    if dec["sustained"] is not None:
+        dec["sustained"]["clocks"] = sampler.summary(*dec["sustained"].pop("window"))
 
     # whole-job value: units of all ranks over the slowest rank's time
     bytes_per_s, ms_step = whole_job(dec["step_bytes"], dec["ms_per_step"], world, dist, dev)
@@ -895,8 +1003,8 @@ def main():
     cpu = None
     if world == 1:
         threads = os.cpu_count() or 1
-        v, desc, secs = oracle_decode_sample(threads)
-        v1, desc1, secs1 = oracle_decode_sample(1, ms=[1])
+        v, desc, secs = oracle_decode_sample(threads, min_seconds=CPU_SAMPLE_S)
+        v1, desc1, secs1 = oracle_decode_sample(1, ms=[1], min_seconds=CPU_SAMPLE_S)
         cpu = {"value": v, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": desc,
                "seconds": round(secs, 2), "host": host_cpu(),
                "one_core": {"value": v1, "sample": desc1, "seconds": round(secs1, 2)}}
@@ -910,7 +1018,7 @@ def main():
                    "l2": f"inputs larger than L2: {LAYERS} layers of FP8 weights "
                          f"({sum(N * K for N, K in SHAPES) * LAYERS / 1e9:.2f} GB) stream once per M per step",
                    "graph": "each step is one CUDA graph replay"},
-        "roofline": dec["roofline"], "cpu_baseline": cpu, "e2e": dec["e2e"],
+        "roofline": dec["roofline"], "cpu_baseline": cpu, "e2e": dec["e2e"], "sustained": dec["sustained"],
         "gpu_launches": dec["launches_per_step"] * args.steps, "clocks": clocks,
         "decode_per_shape": dec["per_shape"], "sections": sections,
         "device_error": {"code": code, "site": site}, "peaks": peaks,

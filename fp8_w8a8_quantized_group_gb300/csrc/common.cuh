@@ -36,6 +36,22 @@ __device__ __forceinline__ uint16_t quant_pair(float a, float b, float s) {
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// Packed BF16 maximum (maxNum: a NaN operand is ignored, as by fmaxf; exact).
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// Running packed amax: m (two BF16 lanes, start at 0) takes the magnitudes
+// of the 8 BF16 values in v; amax_of(m) is the amax so far as a float.
+__device__ __forceinline__ void amax8_acc(uint32_t &m, const uint4 &v) {
+    constexpr uint32_t kAbs = 0x7FFF7FFFu;
+    m = bf16x2_max(m, bf16x2_max(bf16x2_max(v.x & kAbs, v.y & kAbs), bf16x2_max(v.z & kAbs, v.w & kAbs)));
+}
+
+__device__ __forceinline__ float amax_of(uint32_t m) { return fmaxf(bf16lo(m), bf16hi(m)); }
+
 // amax of the 8 BF16 values in a 16-byte vector.
 __device__ __forceinline__ float amax8(const uint4 &v) {
     float a = fabsf(bf16lo(v.x));
@@ -65,40 +81,56 @@ __device__ __forceinline__ uint32_t e4m3_pair(float a, float b) {
     return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
 }
 
-// Same codes as quant8(v, s) - those of the correctly rounded quotients
-// RN(x/s) - for kernels bound by instruction issue, with r = RN(1/s)
-// computed once by the caller. q = RN(x*r) carries two roundings, so it lies
-// within 1.5 * 2^-23 |q| of RN(x/s), while RN(q * (1 -+ 2^-21)) lie more than
-// 3.5 * 2^-23 |q| away on either side: RN(x/s) lies between them. Rounding to
-// nearest even and saturating is monotonic, so when both bounds convert to
-// the codes of q, so does RN(x/s). Otherwise (near a rounding boundary of the
-// conversion), and whenever r overflows (s zero or subnormal, where x*r
-// could be 0 * Inf), the chunk takes correctly rounded divisions.
-__device__ __forceinline__ uint2 quant8_recip(const uint4 &v, float s, float r) {
-    const float x[8] = {bf16lo(v.x), bf16hi(v.x), bf16lo(v.y), bf16hi(v.y),
-                        bf16lo(v.z), bf16hi(v.z), bf16lo(v.w), bf16hi(v.w)};
-    constexpr float kDown = 1.0f - 0x1p-21f, kUp = 1.0f + 0x1p-21f;  // both exact in FP32
-    float q[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) q[i] = __fmul_rn(x[i], r);
-    uint2 out, lo, hi;
-    out.x = e4m3_pair(q[0], q[1]) | (e4m3_pair(q[2], q[3]) << 16);
-    out.y = e4m3_pair(q[4], q[5]) | (e4m3_pair(q[6], q[7]) << 16);
-    lo.x = e4m3_pair(__fmul_rn(q[0], kDown), __fmul_rn(q[1], kDown)) |
-           (e4m3_pair(__fmul_rn(q[2], kDown), __fmul_rn(q[3], kDown)) << 16);
-    lo.y = e4m3_pair(__fmul_rn(q[4], kDown), __fmul_rn(q[5], kDown)) |
-           (e4m3_pair(__fmul_rn(q[6], kDown), __fmul_rn(q[7], kDown)) << 16);
-    hi.x = e4m3_pair(__fmul_rn(q[0], kUp), __fmul_rn(q[1], kUp)) |
-           (e4m3_pair(__fmul_rn(q[2], kUp), __fmul_rn(q[3], kUp)) << 16);
-    hi.y = e4m3_pair(__fmul_rn(q[4], kUp), __fmul_rn(q[5], kUp)) |
-           (e4m3_pair(__fmul_rn(q[6], kUp), __fmul_rn(q[7], kUp)) << 16);
-    if ((lo.x != out.x) | (lo.y != out.y) | (hi.x != out.x) | (hi.y != out.y) | (fabsf(r) == INFINITY)) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) q[i] = __fdiv_rn(x[i], s);
-        out.x = e4m3_pair(q[0], q[1]) | (e4m3_pair(q[2], q[3]) << 16);
-        out.y = e4m3_pair(q[4], q[5]) | (e4m3_pair(q[6], q[7]) << 16);
+// The reciprocal route to the codes of the correctly rounded quotients
+// RN(x/s), for kernels bound by instruction issue. Once per scale:
+// r = RN(1/s), lo = RN(r (1 - 2^-21)), hi = RN(r (1 + 2^-21)). For each x,
+// RN(x lo) and RN(x hi) lie strictly on the two sides of x/s (three roundings
+// of relative size at most 2^-24 each cannot undo the 2^-21 offset; a product
+// small enough to lose that precision gives the code of zero either way), so
+// they bracket RN(x/s). Rounding to E4M3 (nearest even, saturating) is
+// monotonic: when both give the same code, so does RN(x/s). Otherwise (x/s
+// within about 2^-20 of a rounding boundary of the conversion) the chunk takes
+// correctly rounded divisions. When r is not a normal number, or hi
+// overflows, lo = 0 and hi = +Inf: every non-NaN x then disagrees and takes
+// the division.
+struct RecipBracket {
+    float lo, hi;
+};
+
+__device__ __forceinline__ RecipBracket recip_bracket(float s) {
+    const float r = __frcp_rn(s);
+    RecipBracket b{__fmul_rn(r, 1.0f - 0x1p-21f), __fmul_rn(r, 1.0f + 0x1p-21f)};  // both factors exact
+    if (!(fabsf(r) >= 0x1p-126f && fabsf(b.hi) <= 3.402823466e38f)) {
+        b.lo = 0.0f;
+        b.hi = INFINITY;
     }
-    return out;
+    return b;
+}
+
+// The 8 codes of quant8(v, s), in memory order, by the route above (packed
+// FP32 products, two conversions per pair of values).
+__device__ __forceinline__ uint2 quant8_recip(const uint4 &v, float s, RecipBracket b) {
+    const float2 x[4] = {make_float2(bf16lo(v.x), bf16hi(v.x)), make_float2(bf16lo(v.y), bf16hi(v.y)),
+                         make_float2(bf16lo(v.z), bf16hi(v.z)), make_float2(bf16lo(v.w), bf16hi(v.w))};
+    const float2 lo2 = make_float2(b.lo, b.lo), hi2 = make_float2(b.hi, b.hi);
+    float2 p[4], q[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        p[i] = __fmul2_rn(x[i], lo2);
+        q[i] = __fmul2_rn(x[i], hi2);
+    }
+    uint2 lo, hi;
+    lo.x = e4m3_pair(p[0].x, p[0].y) | (e4m3_pair(p[1].x, p[1].y) << 16);
+    lo.y = e4m3_pair(p[2].x, p[2].y) | (e4m3_pair(p[3].x, p[3].y) << 16);
+    hi.x = e4m3_pair(q[0].x, q[0].y) | (e4m3_pair(q[1].x, q[1].y) << 16);
+    hi.y = e4m3_pair(q[2].x, q[2].y) | (e4m3_pair(q[3].x, q[3].y) << 16);
+    if ((lo.x != hi.x) | (lo.y != hi.y)) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) p[i] = make_float2(__fdiv_rn(x[i].x, s), __fdiv_rn(x[i].y, s));
+        lo.x = e4m3_pair(p[0].x, p[0].y) | (e4m3_pair(p[1].x, p[1].y) << 16);
+        lo.y = e4m3_pair(p[2].x, p[2].y) | (e4m3_pair(p[3].x, p[3].y) << 16);
+    }
+    return lo;
 }
 
 __device__ __forceinline__ uint4 ld_stream_v4(const void *p) {

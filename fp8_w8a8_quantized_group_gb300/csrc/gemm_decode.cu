@@ -48,13 +48,16 @@ constexpr int kStages = 5;
 constexpr int kWBytes = kRows * BK;
 constexpr int kXBytes = kTok * BK;
 constexpr int kThreads = 256;
-constexpr int kTmemCols = 32;   // two 16-column partial buffers
+// Two 16-column TMEM partial buffers: the MMA may run one K block ahead of
+// the epilogue (4 and 8 buffers measured the same).
+constexpr int kTBufs = 2;
+constexpr int kTmemCols = kTBufs * kTok < 32 ? 32 : kTBufs * kTok;
 constexpr int kL2Warm = 12;     // weight tiles loaded or warmed in L2 before the upstream grid completes
 constexpr int kScaleKb = 8;     // K blocks of activation/weight scales staged at a time per epilogue warp
 constexpr int kScaleBytes = 4 * 4 * (kScaleKb * kTok + kScaleKb);
 constexpr int kRecvBytes = kRows * kTok * 4;  // split-K partials addressed to this CTA
 constexpr int kSmemBytes =
-    1024 + kStages * (kWBytes + kXBytes) + kRecvBytes + 8 * (2 * kStages + 5) + 16 + kScaleBytes;
+    1024 + kStages * (kWBytes + kXBytes) + kRecvBytes + 8 * (2 * kStages + 2 * kTBufs + 1) + 16 + kScaleBytes;
 
 enum : unsigned { kSiteProdEmpty = 201, kSiteMmaTmem = 202, kSiteMmaFull = 203, kSiteEpiFull = 204,
                   kSiteDrain = 205, kSiteReduce = 206 };
@@ -73,8 +76,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint64_t *full = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(recv) + kRecvBytes);
     uint64_t *empty = full + kStages;
     uint64_t *tfull = empty + kStages;
-    uint64_t *tempty = tfull + 2;
-    uint64_t *rbar = tempty + 2;  // completes when all kRecvBytes have arrived
+    uint64_t *tempty = tfull + kTBufs;
+    uint64_t *rbar = tempty + kTBufs;  // completes when all kRecvBytes have arrived
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(rbar + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     float *scale_smem = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(tmem_slot) + 16);
@@ -89,7 +92,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
-        for (int b = 0; b < 2; ++b) { mbar_init(&tfull[b], 1); mbar_init(&tempty[b], 128); }
+        for (int b = 0; b < kTBufs; ++b) { mbar_init(&tfull[b], 1); mbar_init(&tempty[b], 128); }
         mbar_init(rbar, 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -180,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 last_phase = phase;
                 if (!WHOLE_K || last) {
                     umma_commit(&tfull[buf]);
-                    if (++buf == 2) { buf = 0; bphase ^= 1u; }
+                    if (++buf == kTBufs) { buf = 0; bphase ^= 1u; }
                 }
                 if (++stage == kStages) { stage = 0; phase ^= 1u; }
             }
@@ -237,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     tmem_ld16(lane_addr + buf * kTok, p);
                     tc_fence_before();
                     mbar_arrive(&tempty[buf]);
-                    if (++buf == 2) { buf = 0; bphase ^= 1u; }
+                    if (++buf == kTBufs) { buf = 0; bphase ^= 1u; }
 #pragma unroll
                     for (int j = 0; j < kTok; ++j)
                         if (j < M) acc[j] = fmaf(p[j], wscale * srow[j], acc[j]);

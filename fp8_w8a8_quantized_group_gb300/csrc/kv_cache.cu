@@ -10,11 +10,15 @@
 // paged cache addresses slot = block * block_size + offset.
 //
 // Both kernels are HBM-bound (2 B read + 1 B written per element to store,
-// 1 B read + 2 B written to load): a grid-stride loop of CTAs over token rows,
-// 16-byte BF16 loads and 8-byte code stores (store), 8-byte code loads and
-// 16-byte BF16 stores (load). Codes are e4m3(fl32(x / scale)) through one
-// reciprocal per tensor with the exact fallback of quant8_recip; dequantized
-// values are bf16(fl32(dec(q) * scale)).
+// 1 B read + 2 B written to load): a grid-stride loop of CTAs over groups of
+// kKvTok token rows, 16-byte BF16 loads and 8-byte code stores (store), 8-byte
+// code loads and 16-byte BF16 stores (load). A CTA issues the loads of all
+// kKvTok rows before it stores any (the store's loads do not wait for the
+// slot; the load's wait only for the kKvTok slot reads, issued together), so
+// a thread has 2 kKvTok loads in flight instead of a chain of dependent
+// reads per row. Codes are e4m3(fl32(x / scale)) through one reciprocal per
+// tensor with the exact fallback of quant8_recip; dequantized values are
+// bf16(fl32(dec(q) * scale)).
 #include "common.cuh"
 #include "launch.h"
 
@@ -25,10 +29,13 @@ enum : unsigned { kSiteKvSlot = 401, kSiteKvScale = 402 };
 
 __device__ __forceinline__ bool scale_ok(float s) { return s > 0.0f && s <= 3.402823466e38f; }
 
-// Token t = blockIdx.x (grid-stride) of key and value [tokens][elems] into
-// slot slots[t] of the caches; slots < 0 are padding and skipped, slots at or
-// beyond num_slots are recorded as FP8_ERR_ARG and skipped.
-__global__ void kv_store_kernel(const uint16_t *__restrict__ key, const uint16_t *__restrict__ value,
+constexpr int kKvTok = 4;  // token rows per CTA iteration
+
+// Tokens t0 .. t0 + kKvTok - 1 (t0 = kKvTok * blockIdx.x, grid-stride) of key
+// and value [tokens][elems] into slots slots[t] of the caches; slots < 0 are
+// padding and skipped, slots at or beyond num_slots are recorded as
+// FP8_ERR_ARG and skipped.
+__global__ void __launch_bounds__(256, 4) kv_store_kernel(const uint16_t *__restrict__ key, const uint16_t *__restrict__ value,
                                 uint8_t *__restrict__ kc, uint8_t *__restrict__ vc,
                                 const int64_t *__restrict__ slots, const float *__restrict__ k_scale,
                                 const float *__restrict__ v_scale, int64_t tokens, int64_t elems,
@@ -36,22 +43,34 @@ __global__ void kv_store_kernel(const uint16_t *__restrict__ key, const uint16_t
     grid_dep_wait();
     const float ks = *k_scale, vs = *v_scale;
     if (blockIdx.x == 0 && threadIdx.x == 0 && !(scale_ok(ks) && scale_ok(vs))) record_error(err, kErrArg, kSiteKvScale);
-    const float kr = __frcp_rn(ks), vr = __frcp_rn(vs);
+    const RecipBracket kr = recip_bracket(ks), vr = recip_bracket(vs);
     const int64_t e8 = elems / 8;
-    for (int64_t t = blockIdx.x; t < tokens; t += gridDim.x) {
-        const int64_t slot = __ldg(slots + t);
-        if (slot < 0) continue;
-        if (slot >= num_slots) {
-            if (threadIdx.x == 0) record_error(err, kErrArg, kSiteKvSlot);
-            continue;
-        }
-        const uint16_t *kt = key + t * elems, *vt = value + t * elems;
-        uint8_t *kd = kc + slot * elems, *vd = vc + slot * elems;
+    for (int64_t t0 = static_cast<int64_t>(blockIdx.x) * kKvTok; t0 < tokens;
+         t0 += static_cast<int64_t>(gridDim.x) * kKvTok) {
+        int64_t slot[kKvTok];
+#pragma unroll
+        for (int u = 0; u < kKvTok; ++u) slot[u] = t0 + u < tokens ? __ldg(slots + t0 + u) : -1;
         for (int64_t j = threadIdx.x; j < e8; j += blockDim.x) {
-            const uint4 a = ld_stream_v4(kt + j * 8);
-            const uint4 b = ld_stream_v4(vt + j * 8);
-            *reinterpret_cast<uint2 *>(kd + j * 8) = quant8_recip(a, ks, kr);
-            *reinterpret_cast<uint2 *>(vd + j * 8) = quant8_recip(b, vs, vr);
+            uint4 a[kKvTok], b[kKvTok];
+#pragma unroll
+            for (int u = 0; u < kKvTok; ++u) {
+                a[u] = b[u] = make_uint4(0u, 0u, 0u, 0u);
+                if (t0 + u < tokens) {
+                    a[u] = ld_stream_v4(key + (t0 + u) * elems + j * 8);
+                    b[u] = ld_stream_v4(value + (t0 + u) * elems + j * 8);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kKvTok; ++u) {
+                if (slot[u] < 0 || slot[u] >= num_slots) continue;
+                *reinterpret_cast<uint2 *>(kc + slot[u] * elems + j * 8) = quant8_recip(a[u], ks, kr);
+                *reinterpret_cast<uint2 *>(vc + slot[u] * elems + j * 8) = quant8_recip(b[u], vs, vr);
+            }
+        }
+        if (threadIdx.x == 0) {
+#pragma unroll
+            for (int u = 0; u < kKvTok; ++u)
+                if (slot[u] >= num_slots) record_error(err, kErrArg, kSiteKvSlot);
         }
     }
 }
@@ -83,7 +102,7 @@ __device__ __forceinline__ uint4 dequant8(uint2 c, float s) {
 }
 
 // Row t of the outputs = the dequantized cache slot slots[t] (same skipping
-// rules as the store; skipped rows are not written).
+// rules and token grouping as the store; skipped rows are not written).
 __global__ void kv_load_kernel(const uint8_t *__restrict__ kc, const uint8_t *__restrict__ vc,
                                uint16_t *__restrict__ key, uint16_t *__restrict__ value,
                                const int64_t *__restrict__ slots, const float *__restrict__ k_scale,
@@ -93,20 +112,32 @@ __global__ void kv_load_kernel(const uint8_t *__restrict__ kc, const uint8_t *__
     const float ks = *k_scale, vs = *v_scale;
     if (blockIdx.x == 0 && threadIdx.x == 0 && !(scale_ok(ks) && scale_ok(vs))) record_error(err, kErrArg, kSiteKvScale);
     const int64_t e8 = elems / 8;
-    for (int64_t t = blockIdx.x; t < tokens; t += gridDim.x) {
-        const int64_t slot = __ldg(slots + t);
-        if (slot < 0) continue;
-        if (slot >= num_slots) {
-            if (threadIdx.x == 0) record_error(err, kErrArg, kSiteKvSlot);
-            continue;
-        }
-        const uint8_t *ksrc = kc + slot * elems, *vsrc = vc + slot * elems;
-        uint16_t *kt = key + t * elems, *vt = value + t * elems;
+    for (int64_t t0 = static_cast<int64_t>(blockIdx.x) * kKvTok; t0 < tokens;
+         t0 += static_cast<int64_t>(gridDim.x) * kKvTok) {
+        int64_t slot[kKvTok];
+#pragma unroll
+        for (int u = 0; u < kKvTok; ++u) slot[u] = t0 + u < tokens ? __ldg(slots + t0 + u) : -1;
         for (int64_t j = threadIdx.x; j < e8; j += blockDim.x) {
-            const uint2 a = __ldg(reinterpret_cast<const uint2 *>(ksrc + j * 8));
-            const uint2 b = __ldg(reinterpret_cast<const uint2 *>(vsrc + j * 8));
-            *reinterpret_cast<uint4 *>(kt + j * 8) = dequant8(a, ks);
-            *reinterpret_cast<uint4 *>(vt + j * 8) = dequant8(b, vs);
+            uint2 a[kKvTok], b[kKvTok];
+#pragma unroll
+            for (int u = 0; u < kKvTok; ++u) {
+                a[u] = b[u] = make_uint2(0u, 0u);
+                if (slot[u] >= 0 && slot[u] < num_slots) {
+                    a[u] = __ldg(reinterpret_cast<const uint2 *>(kc + slot[u] * elems + j * 8));
+                    b[u] = __ldg(reinterpret_cast<const uint2 *>(vc + slot[u] * elems + j * 8));
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kKvTok; ++u) {
+                if (slot[u] < 0 || slot[u] >= num_slots) continue;
+                *reinterpret_cast<uint4 *>(key + (t0 + u) * elems + j * 8) = dequant8(a[u], ks);
+                *reinterpret_cast<uint4 *>(value + (t0 + u) * elems + j * 8) = dequant8(b[u], vs);
+            }
+        }
+        if (threadIdx.x == 0) {
+#pragma unroll
+            for (int u = 0; u < kKvTok; ++u)
+                if (slot[u] >= num_slots) record_error(err, kErrArg, kSiteKvSlot);
         }
     }
 }
@@ -123,7 +154,8 @@ cudaError_t launch_kv(const void *fn, int64_t tokens, int64_t elems, void **args
                       cudaStream_t stream) {
     const unsigned threads = kv_threads(elems);
     const int64_t cap = static_cast<int64_t>(dev.sm_count) * (2048 / threads);
-    const int64_t grid = tokens < cap ? tokens : cap;
+    const int64_t groups = (tokens + kKvTok - 1) / kKvTok;
+    const int64_t grid = groups < cap ? groups : cap;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(threads);

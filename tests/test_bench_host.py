@@ -85,7 +85,12 @@ def test_committed_traffic_file_is_well_formed():
 
 
 def test_reference_arm_line(monkeypatch):
-    monkeypatch.setattr(bench, "oracle_decode_sample", lambda threads=None, ms=None, cols=None: (0.25, "a sample", 0.1))
+    calls = []
+
+    def fake(threads=None, ms=None, cols=None, min_seconds=0.0):
+        calls.append(cols)
+        return 0.25, "a sample", 0.1
+    monkeypatch.setattr(bench, "oracle_decode_sample", fake)
     args = types.SimpleNamespace(gpus=1, steps=2, warmup=3)
     out = io.StringIO()
     with redirect_stdout(out):
@@ -99,12 +104,41 @@ def test_reference_arm_line(monkeypatch):
     assert line["e2e"] == {"value": 0.25, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
     host = line["cpu_baseline"]["host"]
     assert host["logical_cpus"] == os.cpu_count() and host["machine"] and isinstance(host["model"], str)
+    # one calibration call on 512 columns, then warmup + steps calls on one column count
+    assert calls[0] == 512 and len(calls) == 1 + 3 + 2 and len(set(calls[1:])) == 1
+
+
+def test_reference_arm_sizes_steps_to_the_run_budget(monkeypatch):
+    """A calibration at 512 columns taking 1 s gives steps of REF_TOTAL_S /
+    (warmup + steps) seconds: the column count scales with it (whole 128-column
+    blocks), and a budget above the full layer runs the full layer."""
+    calls = []
+
+    def fake(threads=None, ms=None, cols=None, min_seconds=0.0):
+        calls.append(cols)
+        return 0.25, "a sample", 1.0
+    monkeypatch.setattr(bench, "oracle_decode_sample", fake)
+    with redirect_stdout(io.StringIO()):
+        bench.reference_arm(types.SimpleNamespace(gpus=1, steps=100, warmup=80))
+    per_step = bench.REF_TOTAL_S / 180
+    assert calls[1] == max(128, int(512 * per_step) // 128 * 128)
+    calls.clear()
+    with redirect_stdout(io.StringIO()):
+        bench.reference_arm(types.SimpleNamespace(gpus=1, steps=1, warmup=0))
+    assert calls[1] is None
 
 
 def test_oracle_sample_runs_on_a_small_slice():
     gbps, desc, seconds = bench.oracle_decode_sample(2, ms=[1, 4], cols=256)
     assert gbps > 0 and seconds > 0
-    assert "[256, 256, 256, 256]" in desc and "2 host thread(s)" in desc
+    assert "[256, 256, 256, 256]" in desc and "2 host thread(s)" in desc and "passes" not in desc
+
+
+def test_oracle_sample_repeats_to_its_minimum_time():
+    _, _, one = bench.oracle_decode_sample(1, ms=[1], cols=128)
+    gbps, desc, seconds = bench.oracle_decode_sample(1, ms=[1], cols=128, min_seconds=2.5 * one)
+    assert seconds >= 2.5 * one and gbps > 0
+    assert "passes" in desc
 
 
 def test_oracle_sample_threads_cover_every_column(monkeypatch):

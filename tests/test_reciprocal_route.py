@@ -1,16 +1,19 @@
-"""The reciprocal route of the weight-block and per-tensor quantizers, checked
-as mathematics on the host (the GPU tests check the kernels themselves).
+"""The reciprocal route of the issue-bound quantizers (weight blocks, per
+tensor, per row, decode-sized activation groups, KV store), checked as
+mathematics on the host (the GPU tests check the kernels themselves).
 
-For a scale s and a value x the kernels take q = RN(x * RN(1/s)) and accept
-its E4M3 code when RN(q * (1 - 2^-21)) and RN(q * (1 + 2^-21)) convert to the
-same code; otherwise they divide. The claim: an accepted code always equals
-the code of the correctly rounded quotient RN(x/s). numpy's float32
-arithmetic is IEEE round-to-nearest-even with subnormals, so it reproduces
-every rounding step; the E4M3 conversion is round-to-nearest-even with
-saturation, here torch's cast of the value clipped to +-448 (the oracle's
-encoder is pinned to that cast within the range). Every BF16 value is tried
-against scales over the whole FP32 range, subnormal and largest included,
-and against scales that put x/s next to a rounding midpoint.
+For a scale s the kernels form r = RN(1/s), lo = RN(r (1 - 2^-21)) and
+hi = RN(r (1 + 2^-21)) once; for each value x they accept the E4M3 code of
+RN(x lo) when RN(x hi) converts to the same code, and divide otherwise (and
+for every x when r is not a normal number or hi overflows). The claim: an
+accepted code always equals the code of the correctly rounded quotient
+RN(x/s). numpy's float32 arithmetic is IEEE round-to-nearest-even with
+subnormals, so it reproduces every rounding step; the E4M3 conversion is
+round-to-nearest-even with saturation, here torch's cast of the value clipped
+to +-448 (the oracle's encoder is pinned to that cast within the range).
+Every BF16 value is tried against scales over the whole FP32 range, subnormal
+and largest included, and against scales that put x/s next to a rounding
+midpoint.
 """
 import numpy as np
 import pytest
@@ -54,6 +57,16 @@ def _scales() -> list[float]:
 SCALES = _scales()
 
 
+def _bracket(s, down, up):
+    """(lo, hi) multipliers of scale s, or None where the kernels divide."""
+    with np.errstate(over="ignore", divide="ignore", under="ignore"):
+        r = np.float32(1.0) / s
+        lo, hi = r * down, r * up
+    if not (abs(r) >= np.float32(2.0 ** -126) and np.isfinite(hi)):
+        return None
+    return lo, hi
+
+
 def _accepted_and_wrong(scales, down, up):
     """(accepted, accepted with a code other than the division's, an example)."""
     x = _all_bf16_values()
@@ -61,16 +74,15 @@ def _accepted_and_wrong(scales, down, up):
     example = None
     for s in scales:
         s = np.float32(s)
-        with np.errstate(over="ignore", invalid="ignore", divide="ignore", under="ignore"):
-            r = np.float32(1.0) / s
-            exact = x / s
-            q = x * r
-            lo, hi = q * down, q * up
-        if not np.isfinite(r):
+        b = _bracket(s, down, up)
+        if b is None:
             continue  # the kernels divide for every element
-        cq = _codes(q)
-        accept = (_codes(lo) == cq) & (_codes(hi) == cq)
-        bad = accept & (cq != _codes(exact))
+        with np.errstate(over="ignore", invalid="ignore", divide="ignore", under="ignore"):
+            exact = x / s
+            lo, hi = x * b[0], x * b[1]
+        clo = _codes(lo)
+        accept = clo == _codes(hi)
+        bad = accept & (clo != _codes(exact))
         accepted += int(accept.sum())
         wrong += int(bad.sum())
         if bad.any() and example is None:
@@ -86,9 +98,9 @@ def test_accepted_codes_equal_the_divided_codes(chunk):
 
 
 def test_a_bracket_too_narrow_to_move_q_is_caught():
-    """The check has teeth: with bounds RN(q (1 -+ 2^-25)), which round back to
-    q itself, every element is accepted, and the same enumeration finds
-    accepted codes that differ from the division's."""
+    """The check has teeth: with multipliers RN(r (1 -+ 2^-25)), which round
+    back to r itself, lo and hi coincide, every element is accepted, and the
+    same enumeration finds accepted codes that differ from the division's."""
     narrow_down, narrow_up = np.float32(1.0 - 2.0 ** -25), np.float32(1.0 + 2.0 ** -25)
     _, wrong, _ = _accepted_and_wrong(SCALES[::4], narrow_down, narrow_up)
     assert wrong > 0
@@ -99,8 +111,14 @@ def test_most_values_take_the_fast_path_at_typical_scales():
     accepted, so the division stays rare."""
     x = synth.bf16_bits_to_f32(synth.to_bf16(np.random.default_rng(5).normal(0.0, 1.0, 65536)))
     s = np.float32(np.abs(x).max() / 448.0)
-    r = np.float32(1.0) / s
-    q = (x * r).astype(np.float32)
-    cq = _codes(q)
-    accept = (_codes(q * DOWN) == cq) & (_codes(q * UP) == cq)
+    lo, hi = _bracket(s, DOWN, UP)
+    accept = _codes((x * lo).astype(np.float32)) == _codes((x * hi).astype(np.float32))
     assert accept.mean() > 0.99
+
+
+def test_scales_with_a_subnormal_reciprocal_divide():
+    """Scales above 2^126 have a subnormal reciprocal, whose relative error is
+    not bounded by 2^-24: the kernels divide there."""
+    for s in (np.float32(3e38), np.float32(2.0 ** 126) * np.float32(1.5), np.float32(3.4028235e38)):
+        assert _bracket(s, DOWN, UP) is None
+    assert _bracket(np.float32(2.0 ** 125), DOWN, UP) is not None
