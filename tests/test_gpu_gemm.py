@@ -58,6 +58,9 @@ def _sample_points(M, N, n_random=4096, seed=0):
     # (every stage loaded before the upstream wait) and one block more (the
     # first refill after those)
     (16, 19584, 640), (5, 19584, 768),
+    # decode split-K with K ranges that do not divide evenly (6, 10 and 14
+    # K blocks over clusters of 4, 8 and 8)
+    (5, 640, 768), (9, 1024, 1280), (11, 896, 1792),
 ])
 def test_block_gemm_full_compare(M, N, K):
     if (M, N, K) == (16, 256, 256):
