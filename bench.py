@@ -891,11 +891,11 @@ def run_case(spec: str, launches: int):
         g.manual_seed(5)
         sl = torch.randperm(N, generator=g, device=dev)[:M].contiguous()
         ks = torch.tensor([0.02], dtype=torch.float32, device=dev)
-        xo = torch.empty_like(x)
+        xv = synth.device_normal_bf16(M, K, 1, "case/V", device=dev)
         if kind == "kvstore":
-            fn = lambda: ops.fp8_kv_cache_store(x, x, kc, vc, sl, ks, ks)  # noqa: E731
+            fn = lambda: ops.fp8_kv_cache_store(x, xv, kc, vc, sl, ks, ks)  # noqa: E731
         else:
-            fn = lambda: ops.fp8_kv_cache_load(kc, vc, x, xo, sl, ks, ks)  # noqa: E731
+            fn = lambda: ops.fp8_kv_cache_load(kc, vc, x, xv, sl, ks, ks)  # noqa: E731
     elif kind == "act":
         qa = torch.empty((M, K), dtype=torch.uint8, device=dev)
         sa = torch.empty((K // 128, M), dtype=torch.float32, device=dev)
