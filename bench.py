@@ -573,7 +573,26 @@ def run_moe_section(torch, ops, dev, steps, warmup, peaks):
     return out
 
 
-def run_quant_section(torch, ops, dev, steps, warmup, peaks):
+def _cpu_quant_times(jobs_host):
+    """The oracle's quantizers on the full shapes on all host cores (row slices
+    of whole blocks per thread; the oracle's C calls release the GIL), each
+    timed once. jobs_host: [(name, fn(lo, hi), rows, row_block)]."""
+    import concurrent.futures as cf
+    threads = os.cpu_count() or 1
+    out = {}
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        for name, fn, rows, rb in jobs_host:
+            blocks = -(-rows // rb)
+            bounds = [rb * (blocks * i // threads) for i in range(threads + 1)]
+            bounds[-1] = rows
+            t0 = time.perf_counter()
+            for f in [ex.submit(fn, a, b) for a, b in zip(bounds[:-1], bounds[1:]) if b > a]:
+                f.result()
+            out[name] = {"us": (time.perf_counter() - t0) * 1e6, "threads": threads}
+    return out
+
+
+def run_quant_section(torch, ops, dev, steps, warmup, peaks, cpu=False):
     x = synth.device_normal_bf16(8192, 14336, 0, "bench/q/X", device=dev)
     qa = torch.empty(x.shape, dtype=torch.uint8, device=dev)
     sa = torch.empty((14336 // 128, 8192), dtype=torch.float32, device=dev)
@@ -596,6 +615,18 @@ def run_quant_section(torch, ops, dev, steps, warmup, peaks):
         out[name] = {"us": t * 1e6, "GBps": nbytes / t / 1e9, "frac_hbm": nbytes / t / 1e9 / peaks["hbm_gbs"]}
     out["note"] = ("inputs larger than L2 (235/235/64 MB); per_tensor_dynamic counts its two reads of the input "
                    "(amax pass + quantize pass)")
+    if cpu:
+        # The CPU oracle on the same full-size inputs (copied to the host
+        # first, outside the timing), for scale: all host cores.
+        import oracle
+        oracle.build()
+        xh = x.view(torch.int16).cpu().numpy().view(np.uint16)
+        wh = w.view(torch.int16).cpu().numpy().view(np.uint16)
+        cpu_t = _cpu_quant_times([
+            ("act_group 8192x14336", lambda a, b: oracle.quant_act_group(xh[a:b]), xh.shape[0], 1),
+            ("weight_block 28672x4096", lambda a, b: oracle.quant_weight_block(wh[a:b]), wh.shape[0], 128)])
+        for name, v in cpu_t.items():
+            out[name]["cpu_oracle"] = {**v, "GBps": [j for j in jobs if j[0] == name][0][2] / (v["us"] * 1e-6) / 1e9}
     return out
 
 
@@ -985,7 +1016,8 @@ def main():
                          ("rowwise", run_rowwise_section), ("kv", run_kv_section)]:
             if name in wanted:
                 torch.cuda.empty_cache()
-                sections[name] = fn(torch, ops, dev, sec_steps, 3, peaks)
+                kw = {"cpu": world == 1} if name == "quant" else {}
+                sections[name] = fn(torch, ops, dev, sec_steps, 3, peaks, **kw)
         code, site = ops.fp8_device_error()
     finally:
         sampler.stop()

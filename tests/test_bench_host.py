@@ -153,3 +153,22 @@ def test_oracle_sample_threads_cover_every_column(monkeypatch):
     monkeypatch.setattr(oracle, "gemm_block", spy)
     bench.oracle_decode_sample(3, ms=[1], cols=640)
     assert sum(seen) == 4 * 640 and all(n % 128 == 0 for n in seen)
+
+
+def test_cpu_quant_times_cover_every_row_once():
+    """The threaded CPU quantizer leg splits rows at whole blocks and covers
+    each row exactly once."""
+    import threading
+    seen = {"w": [], "x": []}
+    lock = threading.Lock()
+
+    def spy(name):
+        def fn(a, b):
+            with lock:
+                seen[name].append((a, b))
+        return fn
+    out = bench._cpu_quant_times([("w", spy("w"), 1000, 128), ("x", spy("x"), 7, 1)])
+    assert set(out) == {"w", "x"} and all(v["us"] > 0 and v["threads"] >= 1 for v in out.values())
+    assert sorted(r for a, b in seen["w"] for r in range(a, b)) == list(range(1000))
+    assert sorted(r for a, b in seen["x"] for r in range(a, b)) == list(range(7))
+    assert all(a % 128 == 0 for a, _ in seen["w"])
