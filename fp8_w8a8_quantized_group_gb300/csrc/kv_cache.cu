@@ -19,7 +19,7 @@
 // reads per row. Codes are e4m3(fl32(x / scale)) through one reciprocal per
 // tensor with the exact fallback of quant8_recip; dequantized values are
 // bf16(fl32(dec(q) * scale)).
-#include "common.cuh"
+#include "quantize.cuh"
 #include "launch.h"
 
 namespace fp8k {

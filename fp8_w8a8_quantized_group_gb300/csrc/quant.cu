@@ -18,14 +18,14 @@
 // The weight-block, per-tensor, row-wise and decode-sized activation
 // quantizers are bound by instruction issue; they reach the correctly rounded
 // quotient's code through one reciprocal bracket per block, row or tensor
-// (recip_bracket / quant8_recip in common.cuh), with a division only near
+// (recip_bracket / quant8_recip in quantize.cuh), with a division only near
 // rounding boundaries, and take amaxes with packed BF16 maxima. Codes are
 // identical to quant8's either way.
 //
 // Every scale is fl32(max(amax, 1e-10) / 448) and every code
 // e4m3(fl32(x / scale)); "[vLLM] FP8" page, sections "스케일링 전략 체계"
 // and "블록 양자화", with the rounding readings stated in fp8w8a8.h.
-#include "common.cuh"
+#include "quantize.cuh"
 #include "launch.h"
 
 namespace fp8k {
