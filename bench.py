@@ -855,8 +855,8 @@ def reference_arm(args):
             "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded SplitMix64/Box-Muller)",
             "config": {"workload": decode_workload(), "parallelism": f"host, {threads} threads",
-                       "sample": "each step one layer of the workload (cpu_baseline.sample), the same sample "
-                                 "as the GPU arm's cpu_baseline"},
+                       "sample": "each step the layer the GPU arm's cpu_baseline samples, on its first output "
+                                 f"columns, sized so that the whole run takes about {REF_TOTAL_S:.0f} s"},
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": desc,
                              "host": host_cpu()},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
