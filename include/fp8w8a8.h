@@ -44,8 +44,11 @@
  *    expires the kernel stops early and records FP8_ERR_TIMEOUT, which
  *    fp8_device_error() reports. Kernels never trap.
  *  - A few arguments can only be checked on the device (a static scale, the
- *    grouped offsets): a bad one is recorded as FP8_ERR_ARG in the same error
- *    word, the call still completes, and its outputs are unspecified.
+ *    grouped offsets, routed-row indices, KV cache slots and scales): a bad
+ *    one is recorded as FP8_ERR_ARG in the same error word with the site that
+ *    found it, the access it would have made is clamped or skipped so that no
+ *    buffer is left, the call still completes, and its outputs are
+ *    unspecified.
  *
  * Programmatic dependent launch (PDL). Some kernels are launched as
  * programmatic dependents of the work before them on the stream, and some
