@@ -109,3 +109,63 @@ def test_weight_block_then_decode_gemm_no_sync():
         qwo, swo = oracle.quant_weight_block(_bits(ws[i][torch.from_numpy(rows).cuda()]))
         yo, ab = oracle.gemm_block(qao, sao, qwo, swo)
         assert_within_tolerance(bf16_to_f64(ys[i])[:, rows], yo, ab, f"iteration {i}")
+
+
+def test_rowwise_weight_then_decode_gemm_no_sync():
+    """fp8_quant_rowwise(W 4096 x 4096, per output channel) -> fp8_rowwise_gemm
+    at M = 1, twenty times with fresh weights, no host sync."""
+    N = K = 4096
+    x, _ = synth.block_case(1, 16, K, seed=4)
+    qa, sa = ops.quant_rowwise(to_dev_bf16(x))
+    qw = torch.empty((N, K), dtype=torch.uint8, device="cuda")
+    sw = torch.empty((N,), dtype=torch.float32, device="cuda")
+    ws, ys = [], []
+    torch.cuda.synchronize()
+    for i in range(ITERS):
+        w = synth.device_normal_bf16(N, K, i, f"order/Wr/{i}", sigma=0.02)
+        ws.append(w)
+        ops.fp8_quant_rowwise(w, qw, sw)
+        y = torch.empty((1, N), dtype=torch.bfloat16, device="cuda")
+        ops.fp8_rowwise_gemm(qa, sa, qw, sw, y)
+        ys.append(y)
+    assert ops.fp8_device_error() == (0, 0)
+    qao, sao = oracle.quant_rowwise(x)
+    for i in range(ITERS):
+        rows = _sample_cols(N, 256, seed=100 + i)  # output channels: per-row quantization is local to a row
+        qwo, swo = oracle.quant_rowwise(_bits(ws[i][torch.from_numpy(rows).cuda()]))
+        yo, ab = oracle.gemm_rowwise(qao, sao, qwo, swo)
+        assert_within_tolerance(bf16_to_f64(ys[i])[:, rows], yo, ab, f"iteration {i}")
+
+
+def test_kv_store_then_load_no_sync():
+    """fp8_kv_cache_store -> fp8_kv_cache_load of the same slots, twenty times
+    with fresh keys and values into one cache, no host sync: every load must
+    see its own store."""
+    T, E, S = 512, 1024, 2048
+    kc = torch.zeros((S, E), dtype=torch.uint8, device="cuda")
+    vc = torch.zeros((S, E), dtype=torch.uint8, device="cuda")
+    ks = torch.tensor([0.02], dtype=torch.float32, device="cuda")
+    vs = torch.tensor([0.015], dtype=torch.float32, device="cuda")
+    g = torch.Generator(device="cuda")
+    g.manual_seed(9)
+    slots = torch.randperm(S, generator=g, device="cuda")[:T].contiguous()
+    keys, vals, kouts, vouts = [], [], [], []
+    torch.cuda.synchronize()
+    for i in range(ITERS):
+        k = synth.device_normal_bf16(T, E, i, f"order/K/{i}")
+        v = synth.device_normal_bf16(T, E, i, f"order/V/{i}")
+        ko = torch.empty_like(k)
+        vo = torch.empty_like(v)
+        ops.fp8_kv_cache_store(k, v, kc, vc, slots, ks, vs)
+        ops.fp8_kv_cache_load(kc, vc, ko, vo, slots, ks, vs)
+        keys.append(k)
+        vals.append(v)
+        kouts.append(ko)
+        vouts.append(vo)
+    assert ops.fp8_device_error() == (0, 0)
+    sl = slots.cpu().numpy()
+    for i in range(ITERS):
+        for x, out, s in ((keys[i], kouts[i], 0.02), (vals[i], vouts[i], 0.015)):
+            cache = oracle.kv_store(_bits(x), sl, np.zeros((S, E), np.uint8), s)
+            ref = oracle.kv_load(cache, sl, np.zeros((T, E), np.uint16), s)
+            assert np.array_equal(_bits(out), ref), f"iteration {i}"
