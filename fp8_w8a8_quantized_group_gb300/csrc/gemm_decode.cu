@@ -52,7 +52,14 @@ constexpr int kThreads = 256;
 // the epilogue (4 and 8 buffers measured the same).
 constexpr int kTBufs = 2;
 constexpr int kTmemCols = kTBufs * kTok < 32 ? 32 : kTBufs * kTok;
-constexpr int kL2Warm = 12;     // weight tiles loaded or warmed in L2 before the upstream grid completes
+// Before the upstream grid completes, the first kStages weight tiles go into
+// their stages and one otherwise idle lane warms the next ones in L2, one tile
+// every kWarmPaceNs, until the upstream wait returns (at most kWarmMax tiles).
+// The amount therefore follows the upstream kernel's remaining time: a short
+// quantizer in front of the GEMM leaves a few microseconds of idle HBM to
+// fill, a previous GEMM that is still streaming leaves none.
+constexpr int kWarmMax = 32;
+constexpr unsigned kWarmPaceNs = 500;
 constexpr int kScaleKb = 8;     // K blocks of activation/weight scales staged at a time per epilogue warp
 constexpr int kScaleBytes = 4 * 4 * (kScaleKb * kTok + kScaleKb);
 constexpr int kRecvBytes = kRows * kTok * 4;  // split-K partials addressed to this CTA
@@ -80,6 +87,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint64_t *rbar = tempty + kTBufs;  // completes when all kRecvBytes have arrived
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(rbar + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    volatile int *waited = reinterpret_cast<volatile int *>(tmem_slot + 2);  // the producer passed the upstream wait
     float *scale_smem = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(tmem_slot) + 16);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -95,6 +103,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int b = 0; b < kTBufs; ++b) { mbar_init(&tfull[b], 1); mbar_init(&tempty[b], 128); }
         mbar_init(rbar, 1);
         *abort_flag = 0;
+        *waited = 0;
         fence_barrier_init();
         if (splits > 1) mbar_arrive_expect_tx(rbar, kRecvBytes);
     }
@@ -120,8 +129,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             // -------------------------------------------------- producer --
             // Weights are read before the upstream wait (the caller's contract:
             // no kernel that triggers this one early writes them): the first
-            // kStages weight tiles go straight into their stages, the next
-            // few are warmed in L2. Activation codes come after the wait.
+            // kStages weight tiles go straight into their stages (warp 3 warms
+            // the next ones in L2). Activation codes come after the wait.
             const uint64_t stream_once = policy_evict_first();
             const int nkb = kb1 - kb0;
             const int pre = nkb < kStages ? nkb : kStages;
@@ -129,10 +138,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                 mbar_arrive_expect_tx(&full[i], kWBytes + kXBytes);
                 tma_load_2d_hint(sW + i * kWBytes, &tmW, &full[i], (kb0 + i) * BK, n0, stream_once);
             }
-            const int warm = nkb < kL2Warm ? nkb : kL2Warm;
-            for (int i = pre; i < warm; ++i) tma_prefetch_l2_2d(&tmW, (kb0 + i) * BK, n0);
             if (splits > 1) cluster_wait_acquire();
             grid_dep_wait();
+            *waited = 1;
             for (int i = 0; i < pre; ++i) tma_load_2d(sX + i * kXBytes, &tmX, &full[i], (kb0 + i) * BK, 0);
             uint32_t stage = static_cast<uint32_t>(pre % kStages), phase = pre == kStages ? 1u : 0u;
             int issued = pre;
@@ -151,6 +159,16 @@ __global__ void __launch_bounds__(kThreads, 2)
                 while (!mbar_try_wait(&full[stage], phase)) {
                     if (global_ns() - t0 > kWaitLimitNs) { record_error(err, kErrTimeout, kSiteDrain); break; }
                 }
+            }
+        }
+    } else if (warp == 3) {
+        if (lane == 0) {
+            // ------------------------------------------------ L2 warming --
+            const int nkb = kb1 - kb0;
+            const int last = nkb < kStages + kWarmMax ? nkb : kStages + kWarmMax;
+            for (int i = kStages; i < last && !*waited; ++i) {
+                tma_prefetch_l2_2d(&tmW, (kb0 + i) * BK, n0);
+                __nanosleep(kWarmPaceNs);
             }
         }
     } else if (warp == 1) {
