@@ -103,8 +103,13 @@ __global__ void __launch_bounds__(kActSmallThreads) quant_act_group_small_kernel
     const int m = ok ? gi / Kg : 0;
     const int g = ok ? gi - m * Kg : 0;
     grid_dep_launch();
-    grid_dep_wait();
     const int64_t off = static_cast<int64_t>(m) * Kg * 128 + g * 128 + c * 8;
+    // Warm this chunk of x in L2 while the upstream kernel finishes. The load
+    // itself waits: x may be that kernel's output. An L2 prefetch brings no
+    // data into the SM and L2 holds the latest value of every line, so it
+    // cannot make the load below see a stale x.
+    if (ok) asm volatile("prefetch.global.L2 [%0];" ::"l"(x + off));
+    grid_dep_wait();
     const uint4 v = ok ? ld_stream_v4(x + off) : make_uint4(0u, 0u, 0u, 0u);
     uint32_t m2 = 0;
     amax8_acc(m2, v);
