@@ -293,23 +293,68 @@ cudaError_t launch_pdl(const void *fn, unsigned grid, unsigned block, void **arg
     return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
-// Whole per-tensor quantization in one CTA (small tensors).
-__global__ void __launch_bounds__(1024) tensor_quant_small_kernel(const uint16_t *__restrict__ x,
-                                                                  uint8_t *__restrict__ q, int64_t n8,
-                                                                  float *scale, int is_static, unsigned *err) {
-    __shared__ float scratch[32];
+// Whole per-tensor quantization of a small tensor (up to kSmallTensor
+// elements) in one cluster of kTcCtas CTAs: each CTA holds its share of x in
+// registers, the CTAs' partial amaxes meet through distributed shared memory,
+// and every CTA quantizes its share with the common scale. One launch, x read
+// once. Launched as a programmatic dependent; it warms its share of x in L2
+// before the upstream wait and lets nothing launch before it completes (its
+// codes may be the weights of a following decode GEMM).
+constexpr int kTcCtas = 8;
+constexpr int kTcThreads = 256;
+constexpr int kTcHeld = 8;  // 16-byte chunks per thread
+static_assert(int64_t(kTcCtas) * kTcThreads * kTcHeld * 8 >= kSmallTensor, "the cluster must cover a small tensor");
+
+__device__ __forceinline__ void cluster_arrive_release() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
+
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// Chunk k of thread t in cluster rank r: (k * kTcCtas + r) * kTcThreads + t, so
+// each CTA reads 4 KB contiguous per k.
+__global__ void __launch_bounds__(kTcThreads) tensor_quant_cluster_kernel(const uint16_t *__restrict__ x,
+                                                                         uint8_t *__restrict__ q, int64_t n8,
+                                                                         float *scale, int is_static,
+                                                                         unsigned *err) {
+    __shared__ float scratch[kTcThreads / 32];
+    __shared__ float cta_amax;
+    const uint32_t rank = cluster_ctarank();
+    const int t = threadIdx.x;
+    auto chunk = [&](int k) { return (static_cast<int64_t>(k) * kTcCtas + rank) * kTcThreads + t; };
+#pragma unroll
+    for (int k = 0; k < kTcHeld; ++k)
+        if (chunk(k) < n8) asm volatile("prefetch.global.L2 [%0];" ::"l"(x + chunk(k) * 8));
+    grid_dep_wait();
+    uint4 v[kTcHeld];
+#pragma unroll
+    for (int k = 0; k < kTcHeld; ++k) v[k] = chunk(k) < n8 ? ld_stream_v4(x + chunk(k) * 8) : make_uint4(0u, 0u, 0u, 0u);
     float sc;
     if (is_static) {
         sc = *scale;
-        if (threadIdx.x == 0) check_static_scale(sc, err, kSiteStaticScaleSmall);
+        if (rank == 0 && t == 0) check_static_scale(sc, err, kSiteStaticScaleSmall);
     } else {
         uint32_t m2 = 0;
-        for (int64_t i = threadIdx.x; i < n8; i += blockDim.x) amax8_acc(m2, ld_stream_v4(x + i * 8));
-        sc = block_scale(block_reduce_max(amax_of(m2), scratch));
+#pragma unroll
+        for (int k = 0; k < kTcHeld; ++k) amax8_acc(m2, v[k]);
+        const float a = block_reduce_max(amax_of(m2), scratch);
+        if (t == 0) cta_amax = a;
+        cluster_arrive_release();  // every CTA's partial is written ...
+        cluster_wait_acquire();    // ... and visible to every CTA of the cluster
+        float g = 0.0f;
+#pragma unroll
+        for (int r = 0; r < kTcCtas; ++r) g = fmaxf(g, ld_cluster_f32(map_shared_rank(smem_u32(&cta_amax), r)));
+        sc = block_scale(g);
+        cluster_arrive_release();  // this CTA is done reading its peers' shared memory
     }
-    for (int64_t i = threadIdx.x; i < n8; i += blockDim.x)
-        *reinterpret_cast<uint2 *>(q + i * 8) = quant8(ld_stream_v4(x + i * 8), sc);
-    if (!is_static && threadIdx.x == 0) *scale = sc;
+    const RecipBracket rc = recip_bracket(sc);
+#pragma unroll
+    for (int k = 0; k < kTcHeld; ++k)
+        if (chunk(k) < n8) *reinterpret_cast<uint2 *>(q + chunk(k) * 8) = quant8_recip(v[k], sc, rc);
+    if (!is_static && rank == 0 && t == 0) *scale = sc;
+    if (!is_static) cluster_wait_acquire();  // no CTA exits while a peer may still read its shared memory
 }
 
 // ---------------------------------------------------- one scale per row --
@@ -425,14 +470,22 @@ cudaError_t launch_quant_per_tensor(const void *x, void *q, float *scale, int64_
     const int64_t n8 = n / 8;  // n is a multiple of 16
     const uint16_t *xp = static_cast<const uint16_t *>(x);
     uint8_t *qp = static_cast<uint8_t *>(q);
-    if (n8 == 0) {
-        if (is_static) return cudaSuccess;
-        tensor_quant_small_kernel<<<1, 32, 0, stream>>>(xp, qp, 0, scale, 0, dev.err);
-        return cudaGetLastError();
-    }
+    if (n8 == 0 && is_static) return cudaSuccess;
     if (n <= kSmallTensor) {
-        tensor_quant_small_kernel<<<1, 1024, 0, stream>>>(xp, qp, n8, scale, is_static ? 1 : 0, dev.err);
-        return cudaGetLastError();
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(kTcCtas);
+        cfg.blockDim = dim3(kTcThreads);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = kTcCtas;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 2;
+        return cudaLaunchKernelEx(&cfg, tensor_quant_cluster_kernel, xp, qp, n8, scale, is_static ? 1 : 0, dev.err);
     }
     // Each pass runs as one resident wave, and the quantize and finalize
     // kernels are programmatic dependents of their predecessors, so their

@@ -108,7 +108,7 @@ def _boundary_static_scales(rng, count):
 
 
 def test_static_per_tensor_multi_cta_boundaries():
-    """All BF16 patterns, tiled past the single-CTA size, through the
+    """All BF16 patterns, tiled past the small-tensor size, through the
     multi-CTA static quantizer at scales on and next to rounding midpoints."""
     x = np.tile(np.arange(65536, dtype=np.uint32).astype(np.uint16), 4).reshape(4096, 64)
     xf = synth.bf16_bits_to_f32(x)
@@ -206,7 +206,7 @@ def test_act_groups_decode_sized_undecided():
 
 
 def test_dynamic_per_tensor_multi_cta_undecided():
-    """Dynamic per-tensor quantization past the single-CTA size: the tensor's
+    """Dynamic per-tensor quantization past the small-tensor size: the tensor's
     amax gives a scale under which a quarter of the values are undecided."""
     rng = np.random.default_rng(25)
     (bits, vals), = _amax_with_undecided(rng, 1, need=64)

@@ -59,7 +59,7 @@ FP8_ERR_ARG = 5
 
 
 @pytest.mark.parametrize("bad", [0.0, -0.5, float("nan"), float("inf")])
-@pytest.mark.parametrize("rows,site", [(8, 302), (2048, 301)])  # single-CTA and multi-kernel paths
+@pytest.mark.parametrize("rows,site", [(8, 302), (2048, 301)])  # small-tensor (one cluster) and multi-kernel paths
 def test_bad_static_scale_is_reported(bad, rows, site):
     """A static per-tensor scale must be positive and finite; only the device
     can read it, so a bad one is recorded in the error word."""
