@@ -372,8 +372,16 @@ __global__ void __launch_bounds__(kRThreads) quant_rows_kernel(const uint16_t *_
                                                                uint8_t *__restrict__ q, float *__restrict__ s,
                                                                int64_t rows, int64_t cols) {
     __shared__ float scratch[kRThreads / 32];
-    grid_dep_wait();
     const int64_t c8 = cols / 8;
+    if (blockIdx.x < rows) {  // warm this CTA's first row in L2 while the upstream kernel finishes
+        const uint16_t *xr = x + static_cast<int64_t>(blockIdx.x) * cols;
+#pragma unroll
+        for (int j = 0; j < kRHeld; ++j) {
+            const int64_t i = threadIdx.x + static_cast<int64_t>(j) * kRThreads;
+            if (i < c8 && (i & 7) == 0) asm volatile("prefetch.global.L2 [%0];" ::"l"(xr + i * 8));
+        }
+    }
+    grid_dep_wait();
     for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
         const uint16_t *xr = x + r * cols;
         uint8_t *qr = q + r * cols;
