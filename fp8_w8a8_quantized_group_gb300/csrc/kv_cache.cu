@@ -16,9 +16,10 @@
 // kKvTok rows before it stores any (the store's loads do not wait for the
 // slot; the load's wait only for the kKvTok slot reads, issued together), so
 // a thread has 2 kKvTok loads in flight instead of a chain of dependent
-// reads per row. Codes are e4m3(fl32(x / scale)) through one reciprocal per
-// tensor with the exact fallback of quant8_recip; dequantized values are
-// bf16(fl32(dec(q) * scale)).
+// reads per row. Codes are e4m3(fl32(x / scale)) by correctly rounded
+// division (quant8; measured faster here than the reciprocal route of the
+// other quantizers: 13.9 against 15.4 us for 8192 tokens of 8 x 128 keys and
+// values); dequantized values are bf16(fl32(dec(q) * scale)).
 #include "quantize.cuh"
 #include "launch.h"
 
@@ -43,7 +44,6 @@ __global__ void __launch_bounds__(256, 4) kv_store_kernel(const uint16_t *__rest
     grid_dep_wait();
     const float ks = *k_scale, vs = *v_scale;
     if (blockIdx.x == 0 && threadIdx.x == 0 && !(scale_ok(ks) && scale_ok(vs))) record_error(err, kErrArg, kSiteKvScale);
-    const RecipBracket kr = recip_bracket(ks), vr = recip_bracket(vs);
     const int64_t e8 = elems / 8;
     for (int64_t t0 = static_cast<int64_t>(blockIdx.x) * kKvTok; t0 < tokens;
          t0 += static_cast<int64_t>(gridDim.x) * kKvTok) {
@@ -63,8 +63,8 @@ __global__ void __launch_bounds__(256, 4) kv_store_kernel(const uint16_t *__rest
 #pragma unroll
             for (int u = 0; u < kKvTok; ++u) {
                 if (slot[u] < 0 || slot[u] >= num_slots) continue;
-                *reinterpret_cast<uint2 *>(kc + slot[u] * elems + j * 8) = quant8_recip(a[u], ks, kr);
-                *reinterpret_cast<uint2 *>(vc + slot[u] * elems + j * 8) = quant8_recip(b[u], vs, vr);
+                *reinterpret_cast<uint2 *>(kc + slot[u] * elems + j * 8) = quant8(a[u], ks);
+                *reinterpret_cast<uint2 *>(vc + slot[u] * elems + j * 8) = quant8(b[u], vs);
             }
         }
         if (threadIdx.x == 0) {

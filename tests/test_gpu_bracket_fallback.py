@@ -1,6 +1,7 @@
 """The exact fallback of the reciprocal route, driven on purpose through every
-kernel that takes the route: the weight-block, per-tensor (multi-CTA path),
-per-row and decode-sized activation quantizers, and the KV cache store.
+kernel that takes the route: the weight-block, per-tensor (small-tensor and
+multi-CTA paths), per-row and decode-sized activation quantizers; the same
+near-midpoint inputs also go through the KV cache store (which divides).
 
 The route accepts the code of RN(x lo) when RN(x hi) converts to the same
 code (lo, hi = RN(RN(1/s) (1 -+ 2^-21))), and otherwise re-quantizes the
