@@ -7,13 +7,16 @@
 //    step, its launch overlaps the previous GEMM and the next GEMM's prologue
 //    overlaps it. Four lanes per group (rather than sixteen) spread the
 //    per-group work - the shuffle amax and the scale division - over 32
-//    elements per lane.
+//    elements per lane. At decode sizes (M <= 16) a kernel with sixteen lanes
+//    per group takes over, and warms its x in L2 before the upstream wait.
 //  - 128 x 128 weight blocks: one CTA per block, the block held in registers
 //    between the amax pass and the quantize pass (read once).
 //  - Per tensor: grid-wide amax (atomicMax on the bit pattern of the
 //    non-negative amax, kept in the output scale slot), then quantize, each
-//    pass one resident wave of CTAs over equal contiguous slices; a
-//    single-CTA kernel does both for small tensors.
+//    pass one resident wave of CTAs over equal contiguous slices; one
+//    cluster of 8 CTAs does both for small tensors (amax through distributed
+//    shared memory).
+//  - One scale per row (per token or per output channel): one CTA per row.
 //
 // The weight-block, per-tensor, row-wise and decode-sized activation
 // quantizers are bound by instruction issue; they reach the correctly rounded
