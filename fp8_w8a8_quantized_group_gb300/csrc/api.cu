@@ -60,10 +60,8 @@ int current_device(const DeviceInfo **out) {
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 
-}  // namespace
-
-CUresult encode_tma_2d_u8(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
-                          uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows) {
+// The driver's tensor-map encoder, resolved once.
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
     std::call_once(g_encode_once, [] {
         void *fn = nullptr;
         cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
@@ -73,13 +71,32 @@ CUresult encode_tma_2d_u8(CUtensorMap *map, const void *base, uint64_t inner, ui
             g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
         }
     });
-    if (g_encode == nullptr) return CUDA_ERROR_NOT_SUPPORTED;
+    return g_encode;
+}
+
+}  // namespace
+
+CUresult encode_tma_2d_u8(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
+                          uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows) {
+    if (encoder() == nullptr) return CUDA_ERROR_NOT_SUPPORTED;
     cuuint64_t dims[2] = {inner, rows};
     cuuint64_t strides[1] = {row_stride_bytes};
     cuuint32_t box[2] = {box_inner, box_rows};
     cuuint32_t elem[2] = {1, 1};
     return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, elem,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+CUresult encode_tma_2d_bf16_sw64(CUtensorMap *map, void *base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+                                 uint32_t box_rows) {
+    if (encoder() == nullptr) return CUDA_ERROR_NOT_SUPPORTED;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t elem[2] = {1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, elem,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 

@@ -22,7 +22,12 @@
 //    32*(w%4).. (the lane quarter the hardware gives that warp) and one half
 //    of the tile's columns; per K block each thread adds
 //    partial * (Sa[m] * Sw) for its row into FP32 registers (the per-block
-//    scale promotion) and, after the last K block, writes its half-row as BF16;
+//    scale promotion). After the last K block the warp's 32 rows leave as BF16
+//    through a 2 KB shared-memory buffer of its own, 32 columns at a time, by
+//    TMA stores: the warp moves on to the next tile's K blocks while the
+//    stores drain (a thread storing its own row instead wrote 32 rows per
+//    instruction and held the promotion, and with it the MMAs, for the
+//    whole drain);
 //  - warpgroup 0 gives registers to the epilogue warpgroups (setmaxnreg);
 //  - per-tensor mode: the MMAs accumulate all of K in TMEM; the epilogue
 //    applies the single scale product once per tile, streaming TMEM to Y;
@@ -45,6 +50,10 @@ constexpr int kThreads = 384;
 constexpr int kEpiThreads = 256;
 constexpr int kMaxGroups = 256;
 constexpr int kTmemCols = 512;
+// Output staging of the block-scaled epilogue: per warp, 32 rows x 32 BF16
+// columns (64-byte rows, 64-byte TMA swizzle), one TMA store box.
+constexpr int kOutCols = 32;
+constexpr int kOutWarpBytes = 32 * kOutCols * 2;
 // Register split: warpgroup 0 shrinks, the two epilogue warpgroups grow.
 // 128 * kLow + 256 * kHigh must not exceed 384 * (registers the kernel is
 // compiled with); the launcher checks that before every launch. The 128 x 256
@@ -73,7 +82,8 @@ struct Cfg {
     static constexpr int kChunk = BN == 128 ? 64 : 32;  // TMEM columns loaded per wait
     static constexpr int kBarrierBytes = 8 * (2 * kStages + 2 * kBufs) + 16;
     static constexpr int kTableBytes = 4 * (3 * kMaxGroups + 2);
-    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarrierBytes + kTableBytes;
+    static constexpr int kOutBytes = 512 + 8 * kOutWarpBytes;  // block-scaled output staging, 512-byte aligned
+    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarrierBytes + kTableBytes + kOutBytes;
 };
 
 // Output tile of a linear tile index: rows [m0, m0+128) of which those below
@@ -140,9 +150,20 @@ __device__ __forceinline__ uint4 pack8_scaled(const float *p, float s) {
     return v;
 }
 
+// Bulk tensor store shared -> global (bulk async-group of the issuing thread).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(map), "r"(x),
+                 "r"(y), "r"(src)
+                 : "memory");
+}
+
+// Wait until this thread's bulk stores have completed (not only read shared memory).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 template <int BN, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmY,
                         const float *__restrict__ sa, const float *__restrict__ sw,
                         __nv_bfloat16 *__restrict__ y, int M, int N, int K, int groups,
                         const int32_t *__restrict__ offsets, int raster, unsigned *err) {
@@ -162,6 +183,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int *t_lo = reinterpret_cast<int *>(tmem_slot + 4);
     int *t_hi = t_lo + kMaxGroups;
     int *t_start = t_hi + kMaxGroups;
+    uint8_t *s_out = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(t_lo) + C::kTableBytes + 511) & ~uintptr_t(511));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int Kg = (K + BK - 1) / BK;
@@ -371,11 +394,48 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (++buf == C::kBufs) { buf = 0; bphase ^= 1u; }
                 }
                 if (!ok) break;
-                if (row_out) {
+                // Output: the warp's 32 rows x kCols columns, kOutCols at a
+                // time, through its 2 KB buffer. Each thread writes its row's
+                // 16-byte chunks in the 64-byte swizzle of the tensor map
+                // (chunk j of row r at j ^ ((r >> 1) & 3)), and lane 0 stores
+                // the 32 x 32 box; TMA leaves out rows >= M and columns >= N.
+                // Before refilling the buffer lane 0 waits until its previous
+                // store has read it. A warp whose rows run past the end of
+                // its expert's range (grouped mode) must not write the next
+                // expert's rows: it reads the buffer back and stores with
+                // plain, guarded stores of 8 rows x 64 bytes each.
+                uint8_t *wbuf = s_out + (warp - 4) * kOutWarpBytes;
+                const int row0 = tl.m0 + quarter * 32;
+                const bool use_tma = row0 + 32 <= tl.row_end || tl.row_end >= M;
 #pragma unroll
-                    for (int c = 0; c < C::kCols / 8; ++c)
-                        if (tl.n0 + c0 + c * 8 < N)
-                            *reinterpret_cast<uint4 *>(yrow + c * 8) = pack8_scaled(acc + c * 8, 1.0f);
+                for (int p = 0; p < C::kCols / kOutCols; ++p) {
+                    if (lane == 0) bulk_wait_read();
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < kOutCols / 8; ++j)
+                        *reinterpret_cast<uint4 *>(wbuf + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
+                            pack8_scaled(acc + p * kOutCols + j * 8, 1.0f);
+                    if (use_tma) {
+                        fence_proxy_async_smem();  // the TMA store reads these writes
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tmY, smem_u32(wbuf), tl.n0 + c0 + p * kOutCols, row0);
+                            bulk_commit();
+                        }
+                    } else {
+                        __syncwarp();
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int rr = (lane >> 2) + 8 * i, jc = lane & 3;
+                            const uint4 v =
+                                *reinterpret_cast<const uint4 *>(wbuf + rr * 64 + ((jc ^ ((rr >> 1) & 3)) << 4));
+                            const int mr = row0 + rr;
+                            const int col = tl.n0 + c0 + p * kOutCols + jc * 8;
+                            if (mr < M && mr < tl.row_end && col < N)
+                                *reinterpret_cast<uint4 *>(y + static_cast<int64_t>(mr) * N + col) = v;
+                        }
+                        __syncwarp();
+                    }
                 }
             } else {
                 ok = __all_sync(0xffffffffu, mbar_wait(&tfull[buf], bphase, abort_flag, err, kSiteEpiFull));
@@ -411,6 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
+    if (!WHOLE_K && warp >= 4 && lane == 0) bulk_wait_all();  // this warp's output stores have landed
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -446,6 +507,8 @@ cudaError_t launch_variant(const void *qa, const float *sa, const void *qw, cons
     if (encode_tma_2d_u8(&tmA, qa, K, M, K, BK, BM) != CUDA_SUCCESS) return cudaErrorInvalidValue;
     const int64_t b_rows = N * (offsets != nullptr ? num_groups : 1);
     if (encode_tma_2d_u8(&tmB, qw, K, b_rows, K, BK, BN) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    CUtensorMap tmY;
+    if (encode_tma_2d_bf16_sw64(&tmY, y, N, M, kOutCols, 32) != CUDA_SUCCESS) return cudaErrorInvalidValue;
 
     int64_t tiles;
     const int64_t num_n = (N + BN - 1) / BN;
@@ -457,7 +520,7 @@ cudaError_t launch_variant(const void *qa, const float *sa, const void *qw, cons
     // smaller one (it stays in L2 while activations stream), else the reverse.
     const int raster = (N <= M) ? 0 : 1;
     gemm_prefill_kernel<BN, MODE><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(
-        tmA, tmB, sa, sw, static_cast<__nv_bfloat16 *>(y), static_cast<int>(M), static_cast<int>(N),
+        tmA, tmB, tmY, sa, sw, static_cast<__nv_bfloat16 *>(y), static_cast<int>(M), static_cast<int>(N),
         static_cast<int>(K), num_groups, offsets, raster, dev.err);
     return cudaGetLastError();
 }

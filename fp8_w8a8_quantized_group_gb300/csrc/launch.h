@@ -19,6 +19,10 @@ struct DeviceInfo {
 // Encoder for tiled TMA descriptors (driver entry point, resolved once).
 CUresult encode_tma_2d_u8(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
                           uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows);
+// BF16 [rows][cols] (row stride cols * 2 bytes), boxes of box_cols x box_rows
+// with 64-byte swizzling (box_cols = 32): the prefill GEMM's output stores.
+CUresult encode_tma_2d_bf16_sw64(CUtensorMap *map, void *base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+                                 uint32_t box_rows);
 
 // 1x128 activation groups. row_index (device int32 [M], or nullptr): row m of
 // q / s is quantized from row row_index[m] of x [M_src][K] (M_src = M without).
