@@ -30,7 +30,8 @@
 //    whole drain);
 //  - warpgroup 0 gives registers to the epilogue warpgroups (setmaxnreg);
 //  - per-tensor mode: the MMAs accumulate all of K in TMEM; the epilogue
-//    applies the single scale product once per tile, streaming TMEM to Y;
+//    applies the single scale product once per tile, streaming TMEM to Y
+//    through the same per-warp buffers and TMA stores;
 //    row/column mode likewise, with sa[m] * sw[n] (per-token activation and
 //    per-channel weight scales).
 //
@@ -50,7 +51,7 @@ constexpr int kThreads = 384;
 constexpr int kEpiThreads = 256;
 constexpr int kMaxGroups = 256;
 constexpr int kTmemCols = 512;
-// Output staging of the block-scaled epilogue: per warp, 32 rows x 32 BF16
+// Output staging of the epilogue: per warp, 32 rows x 32 BF16
 // columns (64-byte rows, 64-byte TMA swizzle), one TMA store box.
 constexpr int kOutCols = 32;
 constexpr int kOutWarpBytes = 32 * kOutCols * 2;
@@ -82,7 +83,7 @@ struct Cfg {
     static constexpr int kChunk = BN == 128 ? 64 : 32;  // TMEM columns loaded per wait
     static constexpr int kBarrierBytes = 8 * (2 * kStages + 2 * kBufs) + 16;
     static constexpr int kTableBytes = 4 * (3 * kMaxGroups + 2);
-    static constexpr int kOutBytes = 512 + 8 * kOutWarpBytes;  // block-scaled output staging, 512-byte aligned
+    static constexpr int kOutBytes = 512 + 8 * kOutWarpBytes;  // output staging of the 8 epilogue warps, 512-byte aligned
     static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarrierBytes + kTableBytes + kOutBytes;
 };
 
@@ -159,6 +160,42 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t sr
 
 // Wait until this thread's bulk stores have completed (not only read shared memory).
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Columns [x, x + 32) of the warp's 32 output rows [row0, row0 + 32), lane l
+// giving row l's four 16-byte chunks of BF16, through the warp's 2 KB buffer
+// wbuf. Each lane writes its chunks in the 64-byte swizzle of the tensor map
+// (chunk j of row r at j ^ ((r >> 1) & 3)), and lane 0 stores the 32 x 32 box;
+// TMA leaves out rows >= M and columns >= N. Before refilling the buffer lane
+// 0 waits until its previous store has read it. With use_tma false (rows that
+// run past the end of an expert's range, which must not be written) the warp
+// reads the buffer back and stores 8 rows x 64 bytes per instruction, each row
+// checked against row_end.
+__device__ __forceinline__ void store_box(const uint4 (&v)[4], uint8_t *wbuf, const CUtensorMap *tmY, int lane,
+                                          int x, int row0, bool use_tma, __nv_bfloat16 *y, int M, int N,
+                                          int row_end) {
+    if (lane == 0) bulk_wait_read();
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4 *>(wbuf + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) = v[j];
+    if (use_tma) {
+        fence_proxy_async_smem();  // the TMA store reads these writes
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(tmY, smem_u32(wbuf), x, row0);
+            bulk_commit();
+        }
+    } else {
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int rr = (lane >> 2) + 8 * i, jc = lane & 3;
+            const uint4 w = *reinterpret_cast<const uint4 *>(wbuf + rr * 64 + ((jc ^ ((rr >> 1) & 3)) << 4));
+            const int mr = row0 + rr, col = x + jc * 8;
+            if (mr < M && mr < row_end && col < N) *reinterpret_cast<uint4 *>(y + static_cast<int64_t>(mr) * N + col) = w;
+        }
+        __syncwarp();
+    }
+}
 
 template <int BN, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -341,8 +378,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const Tile tl = sched.get(t);
             const int m = tl.m0 + r;
             const bool row_in = m < M;
-            const bool row_out = row_in && m < tl.row_end;
-            __nv_bfloat16 *yrow = y + static_cast<int64_t>(m) * N + tl.n0 + c0;
+            const int row0 = tl.m0 + quarter * 32;                     // the warp's first output row
+            uint8_t *const wbuf = s_out + (warp - 4) * kOutWarpBytes;  // its output staging buffer
             if (!WHOLE_K) {
                 float acc[C::kCols];
 #pragma unroll
@@ -394,50 +431,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (++buf == C::kBufs) { buf = 0; bphase ^= 1u; }
                 }
                 if (!ok) break;
-                // Output: the warp's 32 rows x kCols columns, kOutCols at a
-                // time, through its 2 KB buffer. Each thread writes its row's
-                // 16-byte chunks in the 64-byte swizzle of the tensor map
-                // (chunk j of row r at j ^ ((r >> 1) & 3)), and lane 0 stores
-                // the 32 x 32 box; TMA leaves out rows >= M and columns >= N.
-                // Before refilling the buffer lane 0 waits until its previous
-                // store has read it. A warp whose rows run past the end of
-                // its expert's range (grouped mode) must not write the next
-                // expert's rows: it reads the buffer back and stores with
-                // plain, guarded stores of 8 rows x 64 bytes each.
-                uint8_t *wbuf = s_out + (warp - 4) * kOutWarpBytes;
-                const int row0 = tl.m0 + quarter * 32;
+                // Output: the warp's 32 rows, 32 columns at a time.
                 const bool use_tma = row0 + 32 <= tl.row_end || tl.row_end >= M;
 #pragma unroll
-                for (int p = 0; p < C::kCols / kOutCols; ++p) {
-                    if (lane == 0) bulk_wait_read();
-                    __syncwarp();
+                for (int q = 0; q < C::kCols / kOutCols; ++q) {
+                    uint4 v[4];
 #pragma unroll
-                    for (int j = 0; j < kOutCols / 8; ++j)
-                        *reinterpret_cast<uint4 *>(wbuf + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
-                            pack8_scaled(acc + p * kOutCols + j * 8, 1.0f);
-                    if (use_tma) {
-                        fence_proxy_async_smem();  // the TMA store reads these writes
-                        __syncwarp();
-                        if (lane == 0) {
-                            tma_store_2d(&tmY, smem_u32(wbuf), tl.n0 + c0 + p * kOutCols, row0);
-                            bulk_commit();
-                        }
-                    } else {
-                        __syncwarp();
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const int rr = (lane >> 2) + 8 * i, jc = lane & 3;
-                            const uint4 v =
-                                *reinterpret_cast<const uint4 *>(wbuf + rr * 64 + ((jc ^ ((rr >> 1) & 3)) << 4));
-                            const int mr = row0 + rr;
-                            const int col = tl.n0 + c0 + p * kOutCols + jc * 8;
-                            if (mr < M && mr < tl.row_end && col < N)
-                                *reinterpret_cast<uint4 *>(y + static_cast<int64_t>(mr) * N + col) = v;
-                        }
-                        __syncwarp();
-                    }
+                    for (int j = 0; j < 4; ++j) v[j] = pack8_scaled(acc + q * kOutCols + j * 8, 1.0f);
+                    store_box(v, wbuf, &tmY, lane, tl.n0 + c0 + q * kOutCols, row0, use_tma, y, M, N, tl.row_end);
                 }
             } else {
+                const float srow = (MODE == kScaleRowCol && row_in) ? __ldg(sa + m) : 0.0f;
                 ok = __all_sync(0xffffffffu, mbar_wait(&tfull[buf], bphase, abort_flag, err, kSiteEpiFull));
                 if (!ok) break;
                 tc_fence_after();
@@ -449,21 +453,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_fence_before();
                         mbar_arrive(&tempty[buf]);
                     }
-                    if (row_out) {
-                        // Row/column mode: this row's token scale times each
-                        // column's channel scale (loaded per 8 columns).
-                        const float srow = MODE == kScaleRowCol ? __ldg(sa + m) : 0.0f;
 #pragma unroll
-                        for (int q = 0; q < C::kChunk / 8; ++q) {
-                            const int col = c * C::kChunk + q * 8;
-                            if (tl.n0 + c0 + col < N) {
-                                if (MODE == kScaleRowCol)
-                                    *reinterpret_cast<uint4 *>(yrow + col) =
-                                        pack8_rowcol(p + q * 8, srow, sw + tl.n0 + c0 + col);
-                                else
-                                    *reinterpret_cast<uint4 *>(yrow + col) = pack8_scaled(p + q * 8, tensor_scale);
-                            }
+                    for (int q = 0; q < C::kChunk / kOutCols; ++q) {
+                        // Row/column mode: this row's token scale times each
+                        // column's channel scale (loaded per 8 columns; columns
+                        // past N, which the store leaves out, read column 0's).
+                        const int x = tl.n0 + c0 + c * C::kChunk + q * kOutCols;
+                        uint4 v[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const float *pj = p + q * kOutCols + j * 8;
+                            if (MODE == kScaleRowCol)
+                                v[j] = pack8_rowcol(pj, srow, sw + (x + j * 8 < N ? x + j * 8 : 0));
+                            else
+                                v[j] = pack8_scaled(pj, tensor_scale);
                         }
+                        store_box(v, wbuf, &tmY, lane, x, row0, true, y, M, N, M);
                     }
                 }
                 if (++buf == C::kBufs) { buf = 0; bphase ^= 1u; }
@@ -471,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
-    if (!WHOLE_K && warp >= 4 && lane == 0) bulk_wait_all();  // this warp's output stores have landed
+    if (warp >= 4 && lane == 0) bulk_wait_all();  // this warp's output stores have landed
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
