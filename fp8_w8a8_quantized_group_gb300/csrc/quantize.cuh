@@ -48,19 +48,6 @@ __device__ __forceinline__ void amax8_acc(uint32_t &m, const uint4 &v) {
 
 __device__ __forceinline__ float amax_of(uint32_t m) { return fmaxf(bf16lo(m), bf16hi(m)); }
 
-// amax of the 8 BF16 values in a 16-byte vector.
-__device__ __forceinline__ float amax8(const uint4 &v) {
-    float a = fabsf(bf16lo(v.x));
-    a = fmaxf(a, fabsf(bf16hi(v.x)));
-    a = fmaxf(a, fabsf(bf16lo(v.y)));
-    a = fmaxf(a, fabsf(bf16hi(v.y)));
-    a = fmaxf(a, fabsf(bf16lo(v.z)));
-    a = fmaxf(a, fabsf(bf16hi(v.z)));
-    a = fmaxf(a, fabsf(bf16lo(v.w)));
-    a = fmaxf(a, fabsf(bf16hi(v.w)));
-    return a;
-}
-
 // 8 E4M3 codes of the 8 BF16 values in v under scale s, in memory order.
 __device__ __forceinline__ uint2 quant8(const uint4 &v, float s) {
     uint2 r;
@@ -154,7 +141,10 @@ __device__ __forceinline__ void quant_group_by_quad(const uint16_t *x, uint8_t *
         v[i] = make_uint4(0u, 0u, 0u, 0u);
         if (ok) v[i] = ld(x + src + 32 * i);
     }
-    float a = fmaxf(fmaxf(amax8(v[0]), amax8(v[1])), fmaxf(amax8(v[2]), amax8(v[3])));
+    uint32_t m2 = 0;  // packed BF16 maxima of |x| (bit patterns, sign masked)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) amax8_acc(m2, v[i]);
+    float a = amax_of(m2);
     a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
     a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
     if (ok) {
