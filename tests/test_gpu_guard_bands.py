@@ -178,3 +178,40 @@ def test_kv_cache_guarded():
     voo = oracle.kv_load(vco, slots, canary_rows.copy(), 1.0)
     assert np.array_equal(ko.t.view(torch.int16).cpu().numpy().view(np.uint16), koo)
     assert np.array_equal(vo.t.view(torch.int16).cpu().numpy().view(np.uint16), voo)
+
+
+@pytest.mark.parametrize("N", [272, 512])
+def test_grouped_output_at_expert_boundaries(N):
+    """Grouped GEMM whose expert boundaries fall at many row residues mod 32,
+    between canaries, with rows before the first expert and after the last
+    one: a warp whose 32 output rows cross an expert's end stores them with
+    guarded plain stores, every other warp by TMA boxes. Each expert's rows
+    match the oracle; rows outside the experts keep their canary bytes."""
+    K, lead, tail = 256, 5, 3
+    counts = [1, 31, 32, 33, 0, 63, 64, 65, 127, 128, 129, 7]
+    E = len(counts)
+    offsets = np.concatenate([[lead], lead + np.cumsum(counts)]).astype(np.int32)
+    M = int(offsets[-1]) + tail
+    x = synth.activations(M, K, 6, f"guard/edges/X/{N}")
+    qa_h, sa_h = oracle.quant_act_group(x)
+    ws = [synth.weights(N, K, 6, f"guard/edges/W{e}/{N}") for e in range(E)]
+    qw = torch.empty((E, N, K), dtype=torch.uint8, device="cuda")
+    sw = torch.empty((E, (N + 127) // 128, K // 128), dtype=torch.float32, device="cuda")
+    for e in range(E):
+        ops.fp8_quant_weight_block(to_dev_bf16(ws[e]), qw[e], sw[e])
+    y = Guarded((M, N), torch.bfloat16)
+    y.t.view(torch.uint8).fill_(CANARY)
+    ops.fp8_block_gemm(torch.from_numpy(qa_h).cuda(), torch.from_numpy(sa_h).cuda(), qw, sw, y.t, num_groups=E,
+                       group_offsets=torch.from_numpy(offsets).cuda())
+    _check_all((y, "y"))
+    yb = y.t.view(torch.int16).cpu().numpy().view(np.uint16)
+    outside = np.r_[0:lead, int(offsets[-1]):M]
+    assert np.all(yb[outside] == (CANARY << 8) | CANARY), "rows outside the experts were written"
+    yg = bf16_to_f64(y.t)
+    for e in range(E):
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        if r1 == r0:
+            continue
+        qwo, swo = oracle.quant_weight_block(ws[e])
+        yo, ab = oracle.gemm_block(qa_h[r0:r1], np.ascontiguousarray(sa_h[:, r0:r1]), qwo, swo)
+        assert_within_tolerance(yg[r0:r1], yo, ab, f"expert {e}")
